@@ -1,0 +1,402 @@
+"""Benchmark of one tree-verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama7b] [--impl ours|reference]
+
+A step is the whole hot path over one batch of synthetic input, all through
+the C ABI: tree_build -> kv_append -> tree_attention -> verify -> kv_commit.
+Prints ONE JSON line (rank 0). Metric: verified tree nodes per second (the
+speculated-tree nodes, root included, that one step verifies), whole job.
+Under torchrun every rank runs an independent replica on its own GPU (the path
+needs no exchange); value = nodes of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tree nodes/s (tree-attn+verify) on 1 GB300; attn HBM GB/s vs peak"
+L2_BYTES = 129 * 2**20
+DESCR = {
+    "tiny": "Tiny: 1 request, prefix 64, widths (2,2,1) -> 11 nodes, 4 heads x 64, fp32, vocab 256, greedy+MSS",
+    "llama7b": "LLaMA-7B-shaped layer: batch 8, 32 heads x 128, bf16, prefix 2048, widths (1,1,3,1,1,1,1,1) -> 21 "
+               "nodes, greedy verify over vocab 32000",
+    "merge": "merge-based trees: batch 16, 32 heads x 128, bf16, prefixes U[512,4096], 3 chains x 8 merged, MSS "
+             "over vocab 32000",
+    "long65b": "long-context LLaMA-65B-shaped layer: batch 4, 64 heads x 128, bf16, prefix 16384, random tree of "
+               "128 nodes, greedy+MSS over vocab 32000",
+    "opt30b": "OPT-30B-shaped high batch: batch 64, 56 heads x 128, bf16, prefix 1024, widths (2,2,2,2,1) -> 47 "
+              "nodes, MSS over vocab 50272",
+}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def attention_bytes(w) -> int:
+    """Algorithmic bytes of one tree_attention launch: every visible K and V row
+    once (prefix + tree, per head), Q read and the output written once."""
+    esz = 2 if w.dtype == "bf16" else 4
+    n = w.n_nodes_dev
+    kv = sum(int(w.prefix_len[b] + n[b]) for b in range(w.B)) * w.H * w.d * esz * 2
+    qo = int(sum(n)) * w.H * w.d * esz * 2
+    return kv + qo
+
+
+def _traffic_from_profile(w):
+    """dram bytes per attention launch from the committed ncu summary, only if the
+    kernel source is unchanged since the capture (hash of attn_bf16.cu)."""
+    src = os.path.join(ROOT, "tree_speculative_verification_gb300", "csrc", "attn_bf16.cu")
+    prof = os.path.join(ROOT, "profiles", f"tree_attention_{w.name}.md")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        txt = open(prof).read()
+    except OSError:
+        return None
+    kv = {}
+    for line in txt.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, _, v = line[2:].partition(":")
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256_16") != h:
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the GPU is loaded."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.rows, self.proc = [], None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.rows:
+            return None
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            inside = [r for _, r in self.rows]
+            window = "loaded window around the timed region (shorter than one 200 ms sample)"
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        mx = [num(r[2]) for r in inside if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def _oracle_tree(w):
+    import oracle
+    if w.tree_mode == "chains":
+        B, n_max = w.B, w.n_max
+        parent = np.full((B, n_max), -1, np.int32)
+        tokens = np.zeros((B, n_max), np.int32)
+        p_row = np.zeros((B, n_max), np.int32)
+        q_row = np.zeros((B, n_max), np.int32)
+        n_nodes = np.zeros(B, np.int32)
+        for b in range(B):
+            par, tok, src = oracle.merge_chains(w.chains[b], int(w.root_token[b]), n_max)
+            n = len(par)
+            n_nodes[b] = n
+            parent[b, :n], tokens[b, :n], p_row[b, :n], q_row[b, :n] = par, tok, src + 1, np.maximum(src, 0)
+        return parent, tokens, n_nodes, p_row, q_row
+    return w.parent, w.tokens, w.n_nodes, None, w.q_row
+
+
+def run_oracle_sample(w, heads: int, verify: bool = True):
+    """One bounded oracle pass: attention rows of request 0 for `heads` heads,
+    then (optionally) the step's verifier on every request. Returns seconds
+    spent in attention and in verification."""
+    import oracle
+    parent, tokens, n_nodes, p_row, q_row = _oracle_tree(w)
+    n0 = int(n_nodes[0])
+    rows = np.array([(0, h, v) for h in range(heads) for v in range(n0)], np.int32)
+    t0 = time.perf_counter()
+    if w.q is not None and heads > 0:
+        oracle.tree_attention_rows(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.prefix_len, n_nodes, parent, rows,
+                                   nthreads=0)
+    t1 = time.perf_counter()
+    if verify:
+        if w.verify in ("greedy", "both"):
+            oracle.verify_greedy(w.logits, parent, tokens, n_nodes)
+        if w.verify in ("mss", "both"):
+            oracle.verify_mss(w.logits, w.ssm, q_row, w.uniforms, parent, tokens, n_nodes, w.temperature,
+                              p_row=p_row)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, n_nodes
+
+
+def oracle_nodes_per_s(w, budget_s: float):
+    """Time the oracle on a bounded sample and extrapolate to the whole step."""
+    import oracle
+    ta, tv, n_nodes = run_oracle_sample(w, heads=1)
+    heads = max(1, min(w.H, int(budget_s / max(ta, 1e-4))))
+    ta, tv2, n_nodes = run_oracle_sample(w, heads=heads, verify=False)
+    # attention cost per node-head from the sample, applied to every node-head of the step
+    per_node_head = ta / (heads * int(n_nodes[0]))
+    # rows of longer prefixes cost proportionally more keys
+    keys = np.array([w.prefix_len[b] + n_nodes[b] for b in range(w.B)], np.float64)
+    scale = float(np.sum(n_nodes * keys) / (n_nodes[0] * keys[0]))
+    t_step = per_node_head * w.H * int(n_nodes[0]) * scale + tv
+    sample = (f"oracle tree attention for request 0 ({int(n_nodes[0])} nodes) x {heads} of {w.H} heads "
+              f"({ta:.2f} s), scaled by key count to all {w.B} requests and heads; oracle verification of all "
+              f"{w.B} requests ({tv:.2f} s)")
+    return float(np.sum(n_nodes)) / t_step, t_step, oracle.num_threads(), sample
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """--impl reference: the oracle as it stands on the host cores, same config,
+    metric and unit; each step a bounded sample sized to finish in minutes."""
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    from tree_speculative_verification_gb300 import workloads
+    w = workloads.make(args.config)
+    w.n_nodes_dev = _oracle_tree(w)[2]
+    per_step_budget = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_nodes_per_s(w, per_step_budget)
+    vals, times = [], []
+    for _ in range(args.steps):
+        v, t_step, cores, sample = oracle_nodes_per_s(w, per_step_budget)
+        vals.append(v)
+        times.append(t_step)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCR[args.config], "name": args.config},
+            "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    from tree_speculative_verification_gb300 import api, workloads
+    from tree_speculative_verification_gb300.step import DeviceStep
+    api.load_library()
+    w = workloads.make(args.config)
+    s = DeviceStep(w, device)
+    stream = torch.cuda.current_stream(device)
+    kind = w.verify
+    s.run(kind)
+    torch.cuda.synchronize()
+    w.n_nodes_dev = s.tree.n_nodes.cpu().numpy()
+    nodes_per_step = int(w.n_nodes_dev.sum())
+    if s.status.item() not in (0, api.STATUS_ZERO_RESID):
+        raise RuntimeError(f"device status {s.status.item()} after the first step")
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream)
+    for _ in range(args.warmup):
+        s.run(kind)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    t_load0 = time.time()
+    while time.time() - t_load0 < 0.6:      # keep the GPU loaded while the sampler starts
+        for _ in range(20):
+            s.run(kind)
+        torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ver = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        s.build()
+        s.append()
+        att[i][0].record(stream)
+        s.attend()
+        att[i][1].record(stream)
+        ver[i][0].record(stream)
+        s.verify(kind)
+        ver[i][1].record(stream)
+        s.commit(kind)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    t_load1 = time.time()
+    while time.time() - t_load1 < 0.4:
+        for _ in range(20):
+            s.run(kind)
+        torch.cuda.synchronize()
+    if sampler:
+        sampler.stop()
+    ms = ev[0].elapsed_time(ev[1])
+    t_att = sum(a.elapsed_time(b) for a, b in att) / args.steps
+    t_ver = sum(a.elapsed_time(b) for a, b in ver) / args.steps
+    if dist:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = ws * nodes_per_step / (ms_per_step * 1e-3)
+
+    # ---- end to end through the C ABI with host buffers: pinned inputs in, results out
+    e2e = None
+    if rank == 0:
+        e2e = measure_e2e(s, w, kind, args, stream)
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    abytes = attention_bytes(w)
+    achieved = abytes / (t_att * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": _traffic_from_profile(w), "kernel": "tree_attention (k_attn_bf16)",
+            "algorithmic_bytes_per_launch": abytes, "peak_kind": peak_kind,
+            "avg_launch_us": t_att * 1e3}
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, t_step, cores, sample = oracle_nodes_per_s(w, 12.0)
+        cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": sample}
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": DESCR[args.config], "name": args.config, "batch": w.B, "heads": w.H,
+                       "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
+                       "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "l2": f"inputs larger than L2: {abytes / 2**20:.0f} MiB of K/V+Q per step vs 129 MiB"},
+            "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
+            "attention_ms": t_att, "verify_ms": t_ver,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": args.steps * s.launches_per_step(kind)}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def measure_e2e(s, w, kind, args, stream):
+    """Same metric through the public API with HOST buffers: per step, the
+    step's inputs (tokens, prefix lengths, Q / new K / new V, logits and, for
+    MSS, drafter rows and uniforms) go host->device from pinned memory, the
+    step runs, and the verified tokens and counts come back device->host."""
+    import torch
+    pinned = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+    ins = [s.tokens, s.prefix_len, s.q, s.k_new, s.v_new, s.logits]
+    if kind in ("mss", "both"):
+        ins += [s.ssm, s.uniforms]
+    if w.tree_mode == "chains":
+        ins += [s.chains, s.root_token]
+    host_in = [pinned(t) for t in ins]
+    outs = [s.mss_tokens, s.mss_count] if kind == "mss" else [s.out_tokens, s.out_count]
+    outs.append(s.new_prefix_len)
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    steps = max(3, min(args.steps, 200))
+
+    def one():
+        for dev, host in zip(ins, host_in):
+            dev.copy_(host, non_blocking=True)
+        s.run(kind)
+        for host, dev in zip(host_out, outs):
+            host.copy_(dev, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nodes = int(w.n_nodes_dev.sum())
+    return {"value": nodes / (ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="llama7b", choices=sorted(DESCR))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -505,15 +505,17 @@ int or_verify_mss(int B, int n_max, int V, const int32_t *n_nodes, const int32_t
         out_count[b] = 0;
         if (lm_pos) lm_pos[b] = 0;
         if (min_margin) min_margin[b] = INFINITY;
+        /* row indices and tokens are checked for every node up front; finiteness
+         * only for the values the walk reads: the target row of each visited
+         * node, q(x) of each tested child, the whole drafter row of each
+         * rejected child */
         if (!rc)
-            for (int v = 0; v < n && !rc; ++v) {
+            for (int v = 0; v < n; ++v) {
                 int pr = p_row ? p_row[(size_t)b * n_max + v] : v;
                 if (pr < 0 || pr >= NP) rc |= OR_INDEX;
-                else if (!row_finite(logits + ((size_t)b * NP + pr) * V, V)) rc |= OR_NONFINITE;
                 if (par[v] >= 0) {
                     int qr = q_row[(size_t)b * n_max + v];
                     if (qr < 0 || qr >= NQ) rc |= OR_INDEX;
-                    else if (!row_finite(ssm + ((size_t)b * NQ + qr) * V, V)) rc |= OR_NONFINITE;
                     if (tok[v] < 0 || tok[v] >= V) rc |= OR_INDEX;
                 }
             }
@@ -523,19 +525,23 @@ int or_verify_mss(int B, int n_max, int V, const int32_t *n_nodes, const int32_t
         op[0] = u;
         for (;;) {
             int pr = p_row ? p_row[(size_t)b * n_max + u] : u;
+            if (!row_finite(logits + ((size_t)b * NP + pr) * V, V)) { flags |= OR_NONFINITE; break; }
             softmax_t(logits + ((size_t)b * NP + pr) * V, V, temperature, r);
             memcpy(p0, r, sizeof(double) * (size_t)V);
             int k = children_of(n, par, u, ch), next = -1;
             for (int i = 0; i < k; ++i) {
                 int c = ch[i];
                 const float *qc = ssm + ((size_t)b * NQ + q_row[(size_t)b * n_max + c]) * V;
+                if (!isfinite(qc[tok[c]])) { flags |= OR_NONFINITE; break; }
                 double a = accept_prob(OR_MUTANT == 2 ? p0 : r, qc, tok[c]);
                 double mg = fabs((double)ua[c] - a);
                 if (mg < mm) mm = mg;
                 if (mg < margin_eps && first_low < 0) first_low = cnt;
                 if ((double)ua[c] <= a) { next = c; break; }
+                if (!row_finite(qc, V)) { flags |= OR_NONFINITE; break; }
                 if (residual_step(V, r, qc, tok[c])) flags |= OR_ZERO_RESID;
             }
+            if (flags & OR_NONFINITE) break;
             if (next >= 0) {
                 ot[cnt++] = tok[next];
                 op[cnt] = next;
@@ -549,6 +555,7 @@ int or_verify_mss(int B, int n_max, int V, const int32_t *n_nodes, const int32_t
             ot[cnt++] = t;
             break;
         }
+        if (flags & OR_NONFINITE) cnt = 0;
         out_count[b] = cnt;
         if (lm_pos) lm_pos[b] = first_low < 0 ? cnt : first_low;
         if (min_margin) min_margin[b] = mm;

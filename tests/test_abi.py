@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+function that include/treespec.h declares, and rejects bad arguments on the
+host before anything is launched."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from tree_speculative_verification_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treespec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load_library()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert set(api.EXPORTS) == set(names), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert "sm_103a" in api.version()
+
+
+def _tree(B=2, n_max=8):
+    fake = 0x10000    # never dereferenced: every call below fails validation first
+    return api.ts_tree(B, n_max, *([fake] * 9))
+
+
+def test_null_tree_rejected(lib):
+    rc = lib.tree_build(None, None, None, None, None, 0, None, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG
+    assert b"tree" in lib.treespec_last_error()
+
+
+@pytest.mark.parametrize("n_max", [0, 257])
+def test_tree_size_limits(lib, n_max):
+    t = _tree(n_max=n_max)
+    rc = lib.tree_build(C.byref(t), C.c_void_p(0x10000), C.c_void_p(0x10000), C.c_void_p(0x10000), None, 0, None,
+                        None, None)
+    assert rc == api.TS_ERR_INVALID_ARG
+
+
+def test_expansion_larger_than_n_max(lib):
+    t = _tree(n_max=10)
+    w = (C.c_int32 * 3)(2, 2, 1)     # 11 nodes
+    rc = lib.tree_build(C.byref(t), C.c_void_p(0x10000), None, None, w, 3, None, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"n_max" in lib.treespec_last_error()
+
+
+def test_unsupported_head_dim(lib):
+    t = _tree()
+    p = C.c_void_p(0x10000)
+    rc = lib.tree_attention(p, p, p, p, p, C.byref(t), 4, 96, 64, api.TS_BF16, 0.0, p, 1 << 20, None, None)
+    assert rc == api.TS_ERR_UNSUPPORTED
+
+
+def test_misaligned_cache(lib):
+    t = _tree()
+    p, bad = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    rc = lib.tree_attention(p, p, bad, p, p, C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, p, 1 << 20, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
+
+
+def test_workspace_too_small(lib):
+    t = _tree()
+    p = C.c_void_p(0x10000)
+    rc = lib.tree_attention(p, p, p, p, p, C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, p, 0, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"workspace" in lib.treespec_last_error()
+
+
+def test_mss_bad_temperature(lib):
+    t = _tree()
+    p = C.c_void_p(0x10000)
+    rc = lib.verify_mss(p, p, p, p, None, 8, p, p, 1, p, 0.0, C.byref(t), 16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"temperature" in lib.treespec_last_error()
+
+
+def test_commit_alias_rejected(lib):
+    t = _tree()
+    p = C.c_void_p(0x10000)
+    rc = lib.kv_commit(p, p, p, p, p, p, C.byref(t), 2, 128, 64, api.TS_BF16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"alias" in lib.treespec_last_error()
+
+
+def test_chains_too_many_nodes(lib):
+    t = _tree(n_max=24)
+    p = C.c_void_p(0x10000)
+    rc = lib.tree_build_chains(C.byref(t), p, p, 3, 8, None, None, None, None, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    assert api.workspace_size(api.TS_OP_ATTENTION, 8, 32, 21, 128, 2112, 32000) > 0
+    assert api.workspace_size(api.TS_OP_VERIFY_GREEDY, 8, 1, 21, 128, 1, 32000) >= 8 * 21 * 8
+    assert api.workspace_size(api.TS_OP_VERIFY_MSS, 8, 1, 21, 128, 1, 32000) == 0
+    assert api.workspace_size(api.TS_OP_ATTENTION, 8, 32, 300, 128, 2112, 32000) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    saved = api._lib
+    try:
+        api._lib = None
+        with pytest.raises(api.TreespecError):
+            api.load_library(str(tmp_path / "missing.so"))
+    finally:
+        api._lib = saved

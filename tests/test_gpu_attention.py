@@ -1,0 +1,138 @@
+"""GPU parity of tree_attention against the oracle's fp64 TreeAttention(u) =
+Attention(S_u) (SpecInfer Def. 4.1): max-abs error <= 2e-2 for bf16 inputs with
+fp32 accumulation, <= 1e-4 for fp32 inputs.
+
+Small cases cover every kernel variant (node counts 1..256), several key tiles
+with ragged tails, ragged and empty prefixes, and forced key splits; the five
+workloads run at full size in the launch configuration the benchmark times,
+checked on sampled rows."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_speculative_verification_gb300 import api
+from tree_speculative_verification_gb300.step import DeviceStep, to_device
+from tree_speculative_verification_gb300.workloads import f32_to_bf16_bits
+
+from _helpers import attention_error, oracle_tree, sample_rows, workload
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+
+
+def _run_case(rng, B, H, d, n_max, prefix, bf16=True, n_nodes=None, value_scale=1.0):
+    par = np.full((B, n_max), -1, np.int32)
+    n_nodes = np.full(B, n_max, np.int32) if n_nodes is None else np.asarray(n_nodes, np.int32)
+    for b in range(B):
+        for v in range(1, n_nodes[b]):
+            par[b, v] = rng.integers(max(0, v - 6), v)      # deep and wide mixes
+    prefix = np.asarray(prefix, np.int32)
+    L_max = int(prefix.max()) + n_max + int(rng.integers(0, 70))
+    draw = lambda *s: (rng.standard_normal(s) * value_scale).astype(np.float32)
+    q, kn, vn = draw(B, n_max, H, d), draw(B, n_max, H, d), draw(B, n_max, H, d)
+    kc = np.zeros((B, H, L_max, d), np.float32)
+    vc = np.zeros((B, H, L_max, d), np.float32)
+    for b in range(B):
+        kc[b, :, :prefix[b]] = draw(H, int(prefix[b]), d)
+        vc[b, :, :prefix[b]] = draw(H, int(prefix[b]), d)
+    # garbage (NaN) beyond the used rows must not leak into any output
+    for b in range(B):
+        kc[b, :, prefix[b] + n_nodes[b]:] = np.nan
+        vc[b, :, prefix[b] + n_nodes[b]:] = np.nan
+    if bf16:
+        q, kn, vn, kc, vc = map(f32_to_bf16_bits, (q, kn, vn, kc, vc))
+    tok = np.zeros((B, n_max), np.int32)
+    t = api.Tree(B, n_max)
+    api.tree_build(t, to_device(tok, "cuda"), to_device(par, "cuda"), to_device(n_nodes, "cuda"))
+    dv = lambda a: to_device(a, "cuda", bf16)
+    dq, dkn, dvn, dkc, dvc = map(dv, (q, kn, vn, kc, vc))
+    pl = to_device(prefix, "cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.kv_append(dkc, dvc, dkn, dvn, pl, t, st)
+    out = torch.zeros_like(dq)
+    ws = api.workspace(api.TS_OP_ATTENTION, B, H, n_max, d, L_max, 1) if bf16 else None
+    api.tree_attention(out, dq, dkc, dvc, pl, t, 0.0, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rows = oracle.all_rows(B, H, n_nodes)
+    ref = oracle.tree_attention_rows(q, kn, vn, kc, vc, prefix, n_nodes, par, rows)
+    o = out.float().cpu().numpy()
+    got = np.stack([o[b, v, h] for b, h, v in rows])
+    err = float(np.max(np.abs(got - ref)))
+    # the workspace is left zeroed for the next call
+    if ws is not None:
+        cnt_bytes = (B * H * 4 + 255) // 256 * 256
+        assert int(ws[:cnt_bytes].count_nonzero()) == 0
+    return err, o, n_nodes
+
+
+@pytest.mark.parametrize("n_max", [1, 5, 21, 24, 25, 32, 40, 47, 48, 60, 64, 90, 128, 150, 200, 256])
+def test_bf16_every_variant(n_max):
+    rng = np.random.default_rng(n_max)
+    B, H = 2, 3
+    err, _, _ = _run_case(rng, B, H, 128, n_max, prefix=[rng.integers(1, 300), rng.integers(1, 300)])
+    assert err <= TOL_BF16, err
+
+
+@pytest.mark.parametrize("splits", ["1", "2", "5", "64"])
+def test_bf16_forced_splits_ragged(splits, monkeypatch):
+    monkeypatch.setenv("TREESPEC_ATTN_SPLITS", splits)
+    rng = np.random.default_rng(100 + int(splits))
+    B, H, n_max = 4, 2, 21
+    prefix = [0, 63, 64, 1000]
+    n_nodes = [21, 1, 13, 21]
+    err, _, _ = _run_case(rng, B, H, 128, n_max, prefix, n_nodes=n_nodes)
+    assert err <= TOL_BF16, err
+
+
+def test_bf16_head_dim_64():
+    rng = np.random.default_rng(7)
+    err, _, _ = _run_case(rng, 2, 2, 64, 30, prefix=[200, 77])
+    assert err <= TOL_BF16, err
+
+
+def test_bf16_large_scores_stable():
+    # scores of magnitude ~100 exercise the running-max rescaling
+    rng = np.random.default_rng(8)
+    err, _, _ = _run_case(rng, 1, 2, 128, 21, prefix=[700], value_scale=3.0)
+    assert err <= 5 * TOL_BF16, err    # bf16 rounding of inputs of size ~3 scales the error
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_f32_small(d):
+    rng = np.random.default_rng(d)
+    err, _, _ = _run_case(rng, 2, 3, d, 17, prefix=[70, 0], bf16=False)
+    assert err <= TOL_F32, err
+
+
+def test_f32_tiny_workload():
+    w = workload("tiny")
+    s = DeviceStep(w)
+    s.build(); s.append(); s.attend()
+    torch.cuda.synchronize()
+    parent, tokens, n_nodes, _, _ = oracle_tree(w)
+    rows = oracle.all_rows(w.B, w.H, n_nodes)
+    err, _, _ = attention_error(s, w, n_nodes, parent, rows)
+    assert err <= TOL_F32, err
+
+
+@pytest.mark.parametrize("name", ["llama7b", "merge", "long65b", "opt30b"])
+def test_full_size_sampled(name):
+    w = workload(name)
+    s = DeviceStep(w)
+    s.build(); s.append(); s.attend()
+    torch.cuda.synchronize()
+    assert s.status.item() == 0
+    parent, tokens, n_nodes, _, _ = oracle_tree(w)
+    rows = sample_rows(w, n_nodes, 48, seed=len(name))
+    err, _, _ = attention_error(s, w, n_nodes, parent, rows)
+    assert err <= TOL_BF16, err
+    # every output row of every real node is finite
+    out = s.out.float()
+    for b in range(w.B):
+        assert torch.isfinite(out[b, : int(n_nodes[b])]).all()

@@ -385,3 +385,17 @@ def test_mss_bad_q_row_flagged():
                           np.array([[0, 5]], np.int32), np.zeros((1, 2, 2), np.float32),
                           np.array([[-1, 0]]), np.array([[0, 1]]), [2])
     assert r["status"][0] & oracle.OR_INDEX and r["count"][0] == 0
+
+
+def test_mss_nonfinite_only_where_read():
+    V = 4
+    logits = np.zeros((2, 3, V), np.float32)
+    ssm = np.full((2, 1, V), 0.25, np.float32)
+    par = np.array([[-1, 0, 1]] * 2, np.int32)
+    tok = np.array([[0, 1, 2]] * 2, np.int32)
+    uni = np.zeros((2, 2, 3), np.float32)          # every child accepted
+    logits[0, 2, 1] = np.nan                         # on the walk (node 2 is reached)
+    ssm[1, 0, 3] = np.inf                            # drafter row never fully read: children accepted
+    r = oracle.verify_mss(logits, ssm, np.zeros((2, 3), np.int32), uni, par, tok, [3, 3])
+    assert r["status"][0] & oracle.OR_NONFINITE and r["count"][0] == 0
+    assert r["status"][1] == 0 and r["count"][1] == 3

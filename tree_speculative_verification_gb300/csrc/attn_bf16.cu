@@ -1,0 +1,662 @@
+// attn_bf16.cu -- split-KV tree attention, bf16 in / fp32 accumulate.
+//
+// What it computes: TreeAttention(u) = Attention(S_u) for every node u of the
+// token tree (SpecInfer, arXiv 2305.09781, Def. 4.1, Eq. 1-4), all nodes of a
+// (request, head) in one pass over that head's KV cache, whose rows are the
+// verified prefix followed by the tree nodes in depth-first order (sec. 4.2).
+// A key j is visible to node i iff j < P (prefix) or key j - P is an ancestor
+// of i or i itself (the topology-aware causal mask of sec. 4.2); the mask is a
+// bit test on the ancestor bitmask, evaluated in registers.
+//
+// GB300 design:
+//  * The prefix K/V stream is the whole cost (HBM bound). Each CTA owns one
+//    (request, head, key chunk) and streams 64-key K and V tiles with TMA
+//    (cp.async.bulk.tensor, 128-byte swizzle) into a 3-stage mbarrier ring.
+//  * Tensor cores in swap-AB orientation: S^T = K Q^T puts 16 keys on the M
+//    side and the few tree nodes (8 per n-tile) on the N side, so a 21-node
+//    tree pads to 24 columns, not 32 rows. P^T is moved from the accumulator
+//    layout to the B-operand layout with movmatrix; O^T = V^T P^T.
+//  * Online softmax per node column in the exp2 domain; the CTA's partial
+//    (max, sum, O) goes to the workspace and the last CTA of the (request,
+//    head) -- found with an atomic counter, no waiting -- merges the splits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "ts_internal.cuh"
+
+namespace ts {
+namespace {
+
+constexpr int TK = 64;       // keys per pipeline tile
+constexpr int STAGES = 3;
+constexpr int kMaxSplits = 64;
+
+template <int D_, int NT_, int NG_, int KS_>
+struct Cfg {
+    static constexpr int D = D_, NT = NT_, NG = NG_, KS = KS_;
+    static constexpr int WARPS = NG * KS, THREADS = WARPS * 32;
+    static constexpr int NODES = NG * NT * 8;            // node columns held (padded)
+    static constexpr int BOXES = D / 64;                  // 64-column (128-byte) TMA boxes per row
+    static constexpr int BOX_BYTES = TK * 128;
+    static constexpr int TILE_BYTES = BOXES * BOX_BYTES;  // one K or V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int KEYS_PER_WARP = TK / KS;
+    static constexpr int CHUNKS = KEYS_PER_WARP / 16;
+    static constexpr int Q_BYTES = NODES * D * 2;
+    static constexpr int ANC_BYTES = NODES * kMaxWords * 4;
+    static constexpr int NT8P = NT * 8 + 4;               // padded node stride of the merge slots
+    static constexpr int SLOT_FLOATS = 2 * NT * 8 + D * NT8P;
+    static constexpr int OFF_Q = STAGES * STAGE_BYTES;
+    static constexpr int OFF_ANC = OFF_Q + Q_BYTES;
+    static constexpr int OFF_PERM = OFF_ANC + ANC_BYTES;
+    static constexpr int OFF_BAR = OFF_PERM + NODES * 4;
+    static constexpr int OFF_MISC = OFF_BAR + STAGES * 8;
+    static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack for 1024-byte alignment
+    static_assert(NG * (KS - 1) * SLOT_FLOATS * 4 <= STAGES * STAGE_BYTES, "merge slots exceed stage memory");
+    static_assert(KEYS_PER_WARP % 16 == 0, "warp key slice must be a multiple of 16");
+};
+
+// ------------------------------------------------------------ PTX helpers ---
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false after kWaitCycles without completion.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase) {
+    if (mbar_try_wait(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, phase))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &lo_r, float &hi_r) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    lo_r = __bfloat162float(v.x);
+    hi_r = __bfloat162float(v.y);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 128-byte-swizzled byte offset of (row, 16-byte chunk) inside a TMA box.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------- kernel ----
+struct AttnArgs {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *q;
+    const int32_t *prefix_len;
+    ts_tree t;
+    int H, L_max;
+    float scale_log2;
+    int chunk_tiles, splits, n_pad;
+    unsigned *counters;
+    float *part_ml;   // [B*H*splits][2][n_pad]
+    float *part_o;    // [B*H*splits][n_pad][D]
+    uint32_t *status;
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant__ CUtensorMap map_k,
+                                                          const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+    constexpr int D = C::D, NT = C::NT, KS = C::KS;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sm_base = smem_u32(sm);
+    uint32_t *anc_s = (uint32_t *)(sm + C::OFF_ANC);
+    int *perm_s = (int *)(sm + C::OFF_PERM);
+    int *misc = (int *)(sm + C::OFF_MISC);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = warp / KS, ks = warp % KS;
+    const int g = lane >> 2, tq = lane & 3;
+    const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
+    const ts_tree &t = a.t;
+    const int n = t.n_nodes[b], P = a.prefix_len[b];
+    if (n <= 0) return;
+    if (P < 0 || P + n > a.L_max) {
+        if (sidx == 0 && h == 0 && tid == 0) flag(a.status, TS_STATUS_INDEX);
+        return;
+    }
+    const int L = P + n;
+    const int chunk_keys = a.chunk_tiles * TK;
+    const int S_b = (L + chunk_keys - 1) / chunk_keys;
+    if (sidx >= S_b) return;
+    const int k_begin = sidx * chunk_keys, k_end = min(L, k_begin + chunk_keys);
+    const int ntiles = (k_end - k_begin + TK - 1) / TK;
+    const int row0 = (b * a.H + h) * a.L_max + k_begin;
+    const uint32_t bar0 = sm_base + C::OFF_BAR;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](int it) {
+        const int st = it % STAGES;
+        const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
+        const uint32_t bar = bar0 + 8 * st;
+        mbar_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::BOXES; ++bx) {
+            tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row0 + it * TK, bar);
+            tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row0 + it * TK, bar);
+        }
+    };
+    if (tid == 0)
+        for (int it = 0; it < min(STAGES, ntiles); ++it) issue(it);
+
+    // Q rows of the CTA's nodes (DFS order) into swizzled shared memory; ancestor masks
+    const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
+    for (int r = tid; r < C::NODES; r += C::THREADS) perm_s[r] = r < n ? t.perm[(size_t)b * n_max + r] : -1;
+    __syncthreads();
+    {
+        constexpr int CH = D / 8;   // 16-byte chunks per row
+        uint4 *qs = (uint4 *)(sm + C::OFF_Q);
+        for (int idx = tid; idx < C::NODES * CH; idx += C::THREADS) {
+            const int r = idx / CH, c = idx % CH;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < n) {
+                const uint4 *src = (const uint4 *)(a.q + (((size_t)b * n_max + perm_s[r]) * a.H + h) * D);
+                val = src[c];
+            }
+            qs[r * CH + (c ^ (r & 7))] = val;
+        }
+        for (int idx = tid; idx < C::NODES * kMaxWords; idx += C::THREADS) {
+            const int r = idx / kMaxWords, w = idx % kMaxWords;
+            anc_s[idx] = (r < n && w < W) ? t.anc[((size_t)b * n_max + r) * W + w] : 0u;
+        }
+    }
+    __syncthreads();
+
+    // Q as B operand fragments, held in registers for the whole pass
+    const int node0 = grp * NT * 8;
+    uint32_t qf[NT][D / 16][2];
+    {
+        const uint32_t qbase = sm_base + C::OFF_Q;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; kk += 2) {
+                const int r = node0 + j * 8 + (lane & 7);
+                const int c = kk * 2 + (lane >> 3);
+                ldsm_x4(qbase + r * (D * 2) + ((c ^ (r & 7)) << 4), qf[j][kk][0], qf[j][kk][1], qf[j][kk + 1][0],
+                        qf[j][kk + 1][1]);
+            }
+    }
+
+    float oacc[D / 16][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[mt][j][e] = 0.f;
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+    }
+
+    bool timed_out = false;
+    for (int it = 0; it < ntiles; ++it) {
+        const int st = it % STAGES;
+        const uint32_t phase = (uint32_t)(it / STAGES) & 1u;
+        timed_out = !mbar_wait_bounded(bar0 + 8 * st, phase);
+        if (__syncthreads_or(timed_out)) { timed_out = true; break; }
+        const int key_base = k_begin + it * TK;
+        unsigned char *ktile = sm + st * C::STAGE_BYTES;
+        unsigned char *vtile = ktile + C::TILE_BYTES;
+        if (key_base + TK > k_end) {
+            // rows past the chunk may hold anything (even NaN): zero their V so
+            // that a zero probability multiplies a zero
+            for (int idx = tid; idx < TK * C::BOXES * 8; idx += C::THREADS) {
+                const int r = idx / (C::BOXES * 8), rem = idx % (C::BOXES * 8);
+                if (key_base + r >= k_end)
+                    *(uint4 *)(vtile + (rem / 8) * C::BOX_BYTES + r * 128 + (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncthreads();
+        }
+        const uint32_t kb_addr = smem_u32(ktile), vb_addr = smem_u32(vtile);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c) {
+            const int kb = ks * C::KEYS_PER_WARP + c * 16;
+            const int key0 = key_base + kb;
+            if (key0 >= k_end) break;
+            // S^T = K Q^T : 16 keys x (NT*8) nodes
+            float sacc[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int r = kb + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = 2 * (kk & 3) + (lane >> 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb_addr + (kk >> 2) * C::BOX_BYTES + swz(r, ch), a0, a1, a2, a3);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qf[j][kk][0], qf[j][kk][1]);
+            }
+            // mask, scale, column max over the 16 keys
+            float cmax[NT][2];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int key = key0 + g + ((e >> 1) << 3);
+                    const int node = node0 + j * 8 + 2 * tq + (e & 1);
+                    bool vis = key < k_end;
+                    if (vis && key >= P) {
+                        const int tk = key - P;
+                        vis = (anc_s[node * kMaxWords + (tk >> 5)] >> (tk & 31)) & 1u;
+                    }
+                    sacc[j][e] = vis ? sacc[j][e] * a.scale_log2 : -INFINITY;
+                }
+                cmax[j][0] = fmaxf(sacc[j][0], sacc[j][2]);
+                cmax[j][1] = fmaxf(sacc[j][1], sacc[j][3]);
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    float v = cmax[j][x];
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    cmax[j][x] = v;
+                }
+            // online rescale, only when some column's running max moved
+            bool grow = false;
+            float alpha[NT][2], m_use[NT][2];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const float mn = fmaxf(m_run[j][x], cmax[j][x]);
+                    alpha[j][x] = (mn == m_run[j][x]) ? 1.f : exp2f(m_run[j][x] - mn);
+                    grow |= mn != m_run[j][x];
+                    m_run[j][x] = mn;
+                    m_use[j][x] = mn == -INFINITY ? 0.f : mn;
+                }
+            if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    l_run[j][0] *= alpha[j][0];
+                    l_run[j][1] *= alpha[j][1];
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        oacc[mt][j][0] *= alpha[j][0];
+                        oacc[mt][j][1] *= alpha[j][1];
+                        oacc[mt][j][2] *= alpha[j][0];
+                        oacc[mt][j][3] *= alpha[j][1];
+                    }
+                }
+            }
+            // P^T (bf16) in the B-operand layout
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float r0, r1, r2, r3;
+                const uint32_t x0 = pack_bf16(exp2f(sacc[j][0] - m_use[j][0]), exp2f(sacc[j][1] - m_use[j][1]), r0, r1);
+                const uint32_t x1 = pack_bf16(exp2f(sacc[j][2] - m_use[j][0]), exp2f(sacc[j][3] - m_use[j][1]), r2, r3);
+                l_run[j][0] += r0 + r2;
+                l_run[j][1] += r1 + r3;
+                pb[j][0] = movm_t(x0);
+                pb[j][1] = movm_t(x1);
+            }
+            // O^T += V^T P^T
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int r = kb + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = 2 * (mt & 3) + ((lane >> 3) & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb_addr + (mt >> 2) * C::BOX_BYTES + swz(r, ch), a0, a1, a2, a3);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma_bf16(oacc[mt][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+            }
+        }
+        __syncthreads();   // every warp is done with this stage
+        if (tid == 0 && it + STAGES < ntiles) issue(it + STAGES);
+    }
+    if (timed_out) {   // uniform: decided by __syncthreads_or above
+        if (tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
+        return;
+    }
+
+    // ---- merge the KS key-split warps of each node group (through smem)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            float v = l_run[j][x];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            l_run[j][x] = v;
+        }
+    float *slots = (float *)sm;
+    if (KS > 1) {
+        if (ks > 0) {
+            float *sl = slots + (grp * (KS - 1) + (ks - 1)) * C::SLOT_FLOATS;
+            float *sm_m = sl, *sm_l = sl + NT * 8, *sm_o = sl + 2 * NT * 8;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int nc = j * 8 + 2 * tq;
+                if (g == 0) {
+                    sm_m[nc] = m_run[j][0];
+                    sm_m[nc + 1] = m_run[j][1];
+                    sm_l[nc] = l_run[j][0];
+                    sm_l[nc + 1] = l_run[j][1];
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    *(float2 *)(sm_o + (mt * 16 + g) * C::NT8P + nc) = make_float2(oacc[mt][j][0], oacc[mt][j][1]);
+                    *(float2 *)(sm_o + (mt * 16 + g + 8) * C::NT8P + nc) = make_float2(oacc[mt][j][2], oacc[mt][j][3]);
+                }
+            }
+        }
+        __syncthreads();
+        if (ks == 0) {
+            for (int k = 0; k < KS - 1; ++k) {
+                const float *sl = slots + (grp * (KS - 1) + k) * C::SLOT_FLOATS;
+                const float *sm_m = sl, *sm_l = sl + NT * 8, *sm_o = sl + 2 * NT * 8;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int nc = j * 8 + 2 * tq;
+                    float fs[2], fo[2];
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const float mo = sm_m[nc + x];
+                        const float mn = fmaxf(m_run[j][x], mo);
+                        fs[x] = m_run[j][x] == -INFINITY ? 0.f : exp2f(m_run[j][x] - mn);
+                        fo[x] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
+                        l_run[j][x] = l_run[j][x] * fs[x] + sm_l[nc + x] * fo[x];
+                        m_run[j][x] = mn;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const float2 u0 = *(const float2 *)(sm_o + (mt * 16 + g) * C::NT8P + nc);
+                        const float2 u1 = *(const float2 *)(sm_o + (mt * 16 + g + 8) * C::NT8P + nc);
+                        oacc[mt][j][0] = oacc[mt][j][0] * fs[0] + u0.x * fo[0];
+                        oacc[mt][j][1] = oacc[mt][j][1] * fs[1] + u0.y * fo[1];
+                        oacc[mt][j][2] = oacc[mt][j][2] * fs[0] + u1.x * fo[0];
+                        oacc[mt][j][3] = oacc[mt][j][3] * fs[1] + u1.y * fo[1];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    const size_t bh = (size_t)b * a.H + h;
+    if (S_b == 1) {
+        // normalise and write bf16 rows out[b][perm[i]][h][:], staged per warp in smem
+        if (ks == 0) {
+            __nv_bfloat16 *stage = (__nv_bfloat16 *)(sm + C::OFF_Q) + grp * NT * 8 * D;   // Q is no longer needed
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int nc = j * 8 + 2 * tq;
+                const float inv0 = l_run[j][0] > 0.f ? 1.f / l_run[j][0] : 0.f;
+                const float inv1 = l_run[j][1] > 0.f ? 1.f / l_run[j][1] : 0.f;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    stage[nc * D + mt * 16 + g] = __float2bfloat16_rn(oacc[mt][j][0] * inv0);
+                    stage[(nc + 1) * D + mt * 16 + g] = __float2bfloat16_rn(oacc[mt][j][1] * inv1);
+                    stage[nc * D + mt * 16 + g + 8] = __float2bfloat16_rn(oacc[mt][j][2] * inv0);
+                    stage[(nc + 1) * D + mt * 16 + g + 8] = __float2bfloat16_rn(oacc[mt][j][3] * inv1);
+                }
+            }
+            __syncwarp();
+            constexpr int CH = D / 8;
+            for (int idx = lane; idx < NT * 8 * CH; idx += 32) {
+                const int r = idx / CH, c = idx % CH;
+                const int i = node0 + r;
+                if (i < n)
+                    ((uint4 *)(a.out + (((size_t)b * n_max + perm_s[i]) * a.H + h) * D))[c] = ((const uint4 *)stage)[r * CH + c];
+            }
+        }
+        return;
+    }
+
+    // ---- split: publish the partial, the last CTA of (b, h) merges
+    if (ks == 0) {
+        const size_t ps = bh * a.splits + sidx;
+        float *pml = a.part_ml + ps * 2 * a.n_pad;
+        float *po = a.part_o + ps * a.n_pad * D;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int nc = node0 + j * 8 + 2 * tq;
+            if (g == 0) {
+                pml[nc] = m_run[j][0];
+                pml[nc + 1] = m_run[j][1];
+                pml[a.n_pad + nc] = l_run[j][0];
+                pml[a.n_pad + nc + 1] = l_run[j][1];
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                po[(size_t)nc * D + mt * 16 + g] = oacc[mt][j][0];
+                po[(size_t)(nc + 1) * D + mt * 16 + g] = oacc[mt][j][1];
+                po[(size_t)nc * D + mt * 16 + g + 8] = oacc[mt][j][2];
+                po[(size_t)(nc + 1) * D + mt * 16 + g + 8] = oacc[mt][j][3];
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) misc[0] = atomicAdd(&a.counters[bh], 1u) == (unsigned)(S_b - 1);
+    __syncthreads();
+    if (!misc[0]) return;
+    __threadfence();
+    for (int idx = tid; idx < n * (D / 2); idx += C::THREADS) {
+        const int i = idx / (D / 2), dp = (idx % (D / 2)) * 2;
+        float M = -INFINITY;
+        for (int s = 0; s < S_b; ++s) M = fmaxf(M, __ldcg(a.part_ml + (bh * a.splits + s) * 2 * a.n_pad + i));
+        float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+        for (int s = 0; s < S_b; ++s) {
+            const float *pml = a.part_ml + (bh * a.splits + s) * 2 * a.n_pad;
+            const float ms = __ldcg(pml + i);
+            if (ms == -INFINITY) continue;
+            const float f = exp2f(ms - M);
+            Lsum += __ldcg(pml + a.n_pad + i) * f;
+            const float2 ov = __ldcg((const float2 *)(a.part_o + ((bh * a.splits + s) * a.n_pad + i) * D + dp));
+            o0 += ov.x * f;
+            o1 += ov.y * f;
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        *(__nv_bfloat162 *)(a.out + (((size_t)b * n_max + perm_s[i]) * a.H + h) * D + dp) =
+            __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    }
+    if (tid == 0) a.counters[bh] = 0u;   // leave the workspace zeroed
+}
+
+// ------------------------------------------------------------------ host ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *base, int d, long long rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, TK};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Variant {
+    int nodes, threads, smem;
+    const void *fn;
+    cudaError_t (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const AttnArgs &, cudaStream_t);
+};
+
+template <class C>
+cudaError_t launch_cfg(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
+    k_attn_bf16<C><<<grid, C::THREADS, C::SMEM, s>>>(mk, mv, a);
+    return cudaGetLastError();
+}
+
+template <class C>
+Variant variant() {
+    return Variant{C::NODES, C::THREADS, C::SMEM, (const void *)k_attn_bf16<C>, launch_cfg<C>};
+}
+
+template <int D>
+Variant pick(int n_max) {
+    if (n_max <= 24) return variant<Cfg<D, 3, 1, 4>>();
+    if (n_max <= 32) return variant<Cfg<D, 4, 1, 4>>();
+    if (n_max <= 48) return variant<Cfg<D, 3, 2, 4>>();
+    if (n_max <= 64) return variant<Cfg<D, 4, 2, 2>>();
+    if (n_max <= 96) return variant<Cfg<D, 3, 4, 2>>();
+    if (n_max <= 128) return variant<Cfg<D, 4, 4, 2>>();
+    if (n_max <= 192) return variant<Cfg<D, 3, 8, 1>>();
+    return variant<Cfg<D, 4, 8, 1>>();
+}
+
+Variant pick_variant(int d, int n_max) { return d == 64 ? pick<64>(n_max) : pick<128>(n_max); }
+
+int occupancy(const Variant &v) {
+    int occ = 0;
+    cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v.fn, v.threads, v.smem) != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+    }
+    return occ;
+}
+
+}  // namespace
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n > 0 ? n : 152;
+}
+
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
+    AttnPlan p{1, 1, 0, 0};
+    if (dt != TS_BF16) return p;
+    const Variant v = pick_variant(d, n_max);
+    const int tiles = (L_max + TK - 1) / TK;
+    const long long pairs = (long long)B * H;
+    const long long slots = (long long)num_sms() * occupancy(v);
+    int splits = 1;
+    if (pairs < slots) splits = (int)((slots + pairs - 1) / pairs);
+    if (const char *e = getenv("TREESPEC_ATTN_SPLITS")) splits = atoi(e);
+    splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
+    splits = splits > tiles ? tiles : splits;
+    p.chunk_tiles = (tiles + splits - 1) / splits;
+    p.splits = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+    p.n_pad = v.nodes;
+    const size_t counters = ((size_t)pairs * 4 + 255) / 256 * 256;
+    p.ws_bytes = p.splits > 1 ? counters + (size_t)pairs * p.splits * p.n_pad * (2 + d) * 4 : counters;
+    return p;
+}
+
+cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max, float scale,
+                             const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s, const char **why) {
+    const Variant v = pick_variant(d, t.n_max);
+    CUtensorMap mk, mv;
+    const long long rows = (long long)t.B * H * L_max;
+    if (!make_map(&mk, k_cache, d, rows) || !make_map(&mv, v_cache, d, rows)) {
+        *why = "cuTensorMapEncodeTiled failed for the KV cache";
+        return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem);
+    if (e != cudaSuccess) return e;
+    AttnArgs a;
+    a.out = (__nv_bfloat16 *)out;
+    a.q = (const __nv_bfloat16 *)q;
+    a.prefix_len = prefix_len;
+    a.t = t;
+    a.H = H;
+    a.L_max = L_max;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.chunk_tiles = plan.chunk_tiles;
+    a.splits = plan.splits;
+    a.n_pad = plan.n_pad;
+    const size_t pairs = (size_t)t.B * H;
+    const size_t counters = (pairs * 4 + 255) / 256 * 256;
+    a.counters = (unsigned *)ws;
+    a.part_ml = (float *)((char *)ws + counters);
+    a.part_o = a.part_ml + pairs * plan.splits * 2 * plan.n_pad;
+    a.status = status;
+    dim3 grid(plan.splits, H, t.B);
+    return v.launch(grid, mk, mv, a, s);
+}
+
+}  // namespace ts

@@ -1,0 +1,252 @@
+// tree_build.cu -- depth-first linearisation of speculated token trees.
+//
+// SpecInfer (arXiv 2305.09781) sec. 4.2 / Fig. 4: the tree's nodes sit in one
+// KV cache after the verified prefix in depth-first order; sec. 3 / Fig. 3:
+// expansion configuration <k1..km>; Def. 3.2: merge of drafter sequences.
+// "Speculative decoding" concept page, Implementation sketch: position id =
+// prefix length + depth.
+//
+// One CTA of TS_MAX_NODES threads per request; thread v owns input node v.
+// The DFS index of v is the sum, over the nodes on its root path, of
+// 1 + (sizes of the earlier siblings), which needs only subtree sizes and
+// sibling order -- no sequential traversal.
+#include "ts_internal.cuh"
+
+namespace ts {
+namespace {
+
+struct Smem {
+    int par[kMaxNodes];
+    int tok[kMaxNodes];
+    int size[kMaxNodes];
+    int depth[kMaxNodes];
+    int off[kMaxNodes];
+    int dfs[kMaxNodes];
+    int slot_node[kMaxNodes];
+    int roots;
+    int bad;
+};
+
+__device__ void write_empty(const ts_tree &t, int b) {
+    const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
+    for (int i = threadIdx.x; i < n_max; i += blockDim.x) {
+        size_t o = (size_t)b * n_max + i;
+        t.perm[o] = -1;
+        t.dfs_of[o] = -1;
+        t.parent[o] = -1;
+        t.token[o] = -1;
+        t.depth[o] = -1;
+        if (t.pos) t.pos[o] = -1;
+        t.sub_end[o] = -1;
+        for (int w = 0; w < W; ++w) t.anc[o * W + w] = 0u;
+    }
+}
+
+// Linearise the tree held in sm.par / sm.tok (n nodes). Writes every row of
+// request b, including padding, and t.n_nodes[b].
+__device__ void linearize(const ts_tree &t, int b, int n, Smem &sm, int P, uint32_t *status) {
+    const int v = threadIdx.x;
+    if (v == 0) { sm.roots = 0; sm.bad = 0; }
+    __syncthreads();
+    if (v < n) {
+        int p = sm.par[v];
+        if (p == -1) atomicAdd(&sm.roots, 1);
+        else if (p < 0 || p >= n || p == v) sm.bad = 1;
+    }
+    __syncthreads();
+    if (v == 0 && sm.roots != 1) sm.bad = 1;
+    __syncthreads();
+    if (!sm.bad && v < n) {          // every node must reach the root within n steps
+        int u = v, steps = 0;
+        while (sm.par[u] != -1 && steps <= n) { u = sm.par[u]; ++steps; }
+        if (sm.par[u] != -1) sm.bad = 1;
+        sm.depth[v] = steps;
+        sm.size[v] = 1;
+    }
+    __syncthreads();
+    if (sm.bad) {
+        write_empty(t, b);
+        if (v == 0) { t.n_nodes[b] = 0; flag(status, TS_STATUS_BAD_TREE); }
+        return;
+    }
+    if (v < n)   // count v in the subtree of each proper ancestor
+        for (int u = sm.par[v]; u != -1; u = sm.par[u]) atomicAdd(&sm.size[u], 1);
+    __syncthreads();
+    if (v < n) {
+        int p = sm.par[v], o = 0;
+        if (p != -1) {
+            o = 1;
+            for (int w = 0; w < v; ++w)
+                if (sm.par[w] == p) o += sm.size[w];
+        }
+        sm.off[v] = o;
+    }
+    __syncthreads();
+    if (v < n) {
+        int i = 0;
+        for (int u = v; u != -1; u = sm.par[u]) i += sm.off[u];
+        sm.dfs[v] = i;
+    }
+    __syncthreads();
+    const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
+    if (v < n) {
+        const int i = sm.dfs[v];
+        const size_t o = (size_t)b * n_max + i;
+        t.perm[o] = v;
+        t.dfs_of[(size_t)b * n_max + v] = i;
+        t.parent[o] = sm.par[v] < 0 ? -1 : sm.dfs[sm.par[v]];
+        t.token[o] = sm.tok[v];
+        t.depth[o] = sm.depth[v];
+        if (t.pos) t.pos[o] = P + sm.depth[v];
+        t.sub_end[o] = i + sm.size[v];
+        uint32_t words[kMaxWords];
+#pragma unroll
+        for (int w = 0; w < kMaxWords; ++w) words[w] = 0u;
+        for (int u = v; u != -1; u = sm.par[u]) {
+            int j = sm.dfs[u];
+            words[j >> 5] |= 1u << (j & 31);
+        }
+        for (int w = 0; w < W; ++w) t.anc[o * W + w] = words[w];
+    } else if (v < n_max) {
+        const size_t o = (size_t)b * n_max + v;
+        t.perm[o] = -1;
+        t.dfs_of[o] = -1;
+        t.parent[o] = -1;
+        t.token[o] = -1;
+        t.depth[o] = -1;
+        if (t.pos) t.pos[o] = -1;
+        t.sub_end[o] = -1;
+        for (int w = 0; w < W; ++w) t.anc[o * W + w] = 0u;
+    }
+    if (v == 0) t.n_nodes[b] = n;
+}
+
+__global__ void __launch_bounds__(kMaxNodes) k_build_parent(ts_tree t, const int32_t *tokens,
+                                                            const int32_t *parent, const int32_t *n_nodes,
+                                                            const int32_t *prefix_len, uint32_t *status) {
+    __shared__ Smem sm;
+    const int b = blockIdx.x, v = threadIdx.x;
+    const int n = n_nodes[b];
+    const int P = prefix_len ? prefix_len[b] : 0;
+    if (n < 1 || n > t.n_max) {
+        __syncthreads();
+        write_empty(t, b);
+        if (v == 0) { t.n_nodes[b] = 0; flag(status, TS_STATUS_BAD_TREE); }
+        return;
+    }
+    if (v < n) {
+        sm.par[v] = parent[(size_t)b * t.n_max + v];
+        sm.tok[v] = tokens[(size_t)b * t.n_max + v];
+    }
+    __syncthreads();
+    linearize(t, b, n, sm, P, status);
+}
+
+__global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int32_t *tokens, WidthsParam w,
+                                                            const int32_t *prefix_len, uint32_t *status) {
+    __shared__ Smem sm;
+    const int b = blockIdx.x, v = threadIdx.x;
+    const int n = w.n;
+    const int P = prefix_len ? prefix_len[b] : 0;
+    if (v < n) {
+        int p = -1;
+        for (int l = 1; l <= w.m; ++l)
+            if (v >= w.level_start[l] && v < w.level_start[l + 1])
+                p = w.level_start[l - 1] + (v - w.level_start[l]) / w.width[l - 1];
+        sm.par[v] = p;
+        sm.tok[v] = tokens[(size_t)b * t.n_max + v];
+    }
+    __syncthreads();
+    linearize(t, b, n, sm, P, status);
+}
+
+// Def. 3.2 merge, data-parallel: slot s = (chain c, position p). The slot
+// opens a new node iff no earlier chain holds the same tokens 0..p; the new
+// nodes are numbered by slot order (creation order), the root being node 0.
+__global__ void __launch_bounds__(kMaxNodes) k_build_chains(ts_tree t, const int32_t *root_token,
+                                                            const int32_t *chains, int C, int len,
+                                                            int32_t *tokens_out, int32_t *p_row,
+                                                            int32_t *q_row, const int32_t *prefix_len,
+                                                            uint32_t *status) {
+    __shared__ Smem sm;
+    __shared__ int is_new[kMaxNodes];
+    __shared__ int canon[kMaxNodes];
+    __shared__ int n_sh;
+    const int b = blockIdx.x, s = threadIdx.x;
+    const int S = C * len;
+    const int32_t *ch = chains + (size_t)b * S;
+    const int P = prefix_len ? prefix_len[b] : 0;
+    if (s < S) {
+        const int c = s / len, p = s % len;
+        int cs = c;
+        for (int c2 = 0; c2 < c; ++c2) {
+            bool same = true;
+            for (int q = 0; q <= p && same; ++q) same = ch[c2 * len + q] == ch[c * len + q];
+            if (same) { cs = c2; break; }
+        }
+        canon[s] = cs * len + p;
+        is_new[s] = cs == c;
+    }
+    __syncthreads();
+    if (s < S && is_new[s]) {
+        int id = 1;
+        for (int s2 = 0; s2 < s; ++s2) id += is_new[s2];
+        sm.slot_node[s] = id;
+    }
+    __syncthreads();
+    if (s < S && !is_new[s]) sm.slot_node[s] = sm.slot_node[canon[s]];
+    if (s == 0) {
+        int cnt = 1;
+        for (int s2 = 0; s2 < S; ++s2) cnt += is_new[s2];
+        n_sh = cnt;
+    }
+    __syncthreads();
+    const int n = n_sh;
+    const size_t base = (size_t)b * t.n_max;
+    if (s < S && is_new[s]) {
+        const int v = sm.slot_node[s], p = s % len;
+        sm.par[v] = p == 0 ? 0 : sm.slot_node[s - 1];
+        sm.tok[v] = ch[s];
+        if (p_row) p_row[base + v] = 1 + s;
+        if (q_row) q_row[base + v] = s;
+    }
+    if (s == 0) {
+        sm.par[0] = -1;
+        sm.tok[0] = root_token[b];
+        if (p_row) p_row[base] = 0;
+        if (q_row) q_row[base] = -1;
+    }
+    for (int v = n + s; v < t.n_max; v += blockDim.x) {
+        if (p_row) p_row[base + v] = -1;
+        if (q_row) q_row[base + v] = -1;
+        if (tokens_out) tokens_out[base + v] = -1;
+    }
+    __syncthreads();
+    if (tokens_out && s < n) tokens_out[base + s] = sm.tok[s];
+    linearize(t, b, n, sm, P, status);
+}
+
+}  // namespace
+
+cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
+                                     const int32_t *n_nodes, const int32_t *prefix_len, uint32_t *status,
+                                     cudaStream_t s) {
+    k_build_parent<<<t.B, kMaxNodes, 0, s>>>(t, tokens, parent, n_nodes, prefix_len, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_build_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
+                                     const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
+    k_build_widths<<<t.B, kMaxNodes, 0, s>>>(t, tokens, w, prefix_len, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token, const int32_t *chains, int C,
+                                     int len, int32_t *tokens_out, int32_t *p_row, int32_t *q_row,
+                                     const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
+    k_build_chains<<<t.B, kMaxNodes, 0, s>>>(t, root_token, chains, C, len, tokens_out, p_row, q_row,
+                                             prefix_len, status);
+    return cudaGetLastError();
+}
+
+}  // namespace ts

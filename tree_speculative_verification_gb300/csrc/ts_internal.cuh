@@ -1,0 +1,73 @@
+// ts_internal.cuh -- shared internals of libtreespec (kernel launchers, device helpers).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/treespec.h"
+
+namespace ts {
+
+constexpr int kMaxNodes = TS_MAX_NODES;
+constexpr int kMaxWords = TS_MASK_WORDS(TS_MAX_NODES);
+
+// Bounded waits: a spin gives up after this many clock64 cycles (about 2 s at
+// 2 GHz), records TS_STATUS_TIMEOUT and lets the kernel return.
+constexpr long long kWaitCycles = 4000000000LL;
+
+__device__ __forceinline__ void flag(uint32_t *status, uint32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---- launchers (one per .cu file) -------------------------------------------
+struct WidthsParam {
+    int m;
+    int n;                 // total node count
+    int level_start[17];   // start id of each level, level_start[m+1] = n
+    int width[16];
+};
+
+cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
+                                     const int32_t *n_nodes, const int32_t *prefix_len,
+                                     uint32_t *status, cudaStream_t s);
+cudaError_t launch_tree_build_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
+                                     const int32_t *prefix_len, uint32_t *status, cudaStream_t s);
+cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token, const int32_t *chains,
+                                     int C, int len, int32_t *tokens_out, int32_t *p_row, int32_t *q_row,
+                                     const int32_t *prefix_len, uint32_t *status, cudaStream_t s);
+
+cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
+                             int esize, uint32_t *status, cudaStream_t s);
+cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int32_t *new_prefix_len,
+                             const int32_t *out_path, const int32_t *out_count, const ts_tree &t, int H,
+                             int d, int L_max, int esize, uint32_t *status, cudaStream_t s);
+
+// Split-KV plan shared by the size query and the launch.
+struct AttnPlan {
+    int splits;        // CTAs per (b, h) at most
+    int chunk_tiles;   // 64-key tiles per CTA
+    int n_pad;         // node rows kept per partial
+    size_t ws_bytes;   // partials + counters
+};
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
+
+cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, const float *v_cache,
+                            const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
+                            float scale, uint32_t *status, cudaStream_t s);
+cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
+                             float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,
+                             const char **why);
+
+size_t greedy_ws_bytes(int B, int n_max, int V);
+cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+                                 int32_t *argmax_out, const float *logits, const ts_tree &t, int V, void *ws,
+                                 uint32_t *status, cudaStream_t s);
+cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+                              const float *logits, const int32_t *p_row, int NP, const float *ssm,
+                              const int32_t *q_row, int NQ, const float *uniforms, float temperature,
+                              const ts_tree &t, int V, uint32_t *status, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace ts

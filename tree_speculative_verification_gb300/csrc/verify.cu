@@ -1,0 +1,539 @@
+// verify.cu -- tree verification kernels (SpecInfer, arXiv 2305.09781, sec. 4.3,
+// Algorithm 2: VerifyGreedy and VerifyStochastic / multi-step speculative
+// sampling; residual norm(max(0, p - q)) as in "How Speculative Decoding in
+// LLM Serving Actually Works").
+//
+// verify_greedy: node-parallel. Every (request, node, vocab segment) CTA
+//   streams its slice of the target logits once (argmax, lowest id on ties);
+//   the last CTA of a request merges the segments and walks the tree.
+// verify_mss: walk-first. One 1024-thread CTA per request follows Algorithm 2
+//   and touches only the rows on the accepted path (the target row of each
+//   visited node, the drafter rows of its tested children); each step is a
+//   block-wide reduction over the vocabulary. Elementwise work is fp32; sums
+//   are per-thread compensated (Kahan) fp32, merged as float-float across a
+//   warp and in fp64 across warps.
+#include <float.h>
+#include <math.h>
+
+#include "ts_internal.cuh"
+
+namespace ts {
+namespace {
+
+// ---------------------------------------------------------------- greedy ----
+constexpr int kGreedyThreads = 256;
+constexpr int kMaxSeg = 8;
+
+struct ArgPart {
+    float val;
+    int idx;   // -1: the segment held a non-finite value
+};
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void consider(float x, int i, float &bv, int &bi, bool &nf) {
+    if (!isfinite(x)) nf = true;
+    if (x > bv) { bv = x; bi = i; }   // indices arrive in increasing order per thread
+}
+
+__global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, int32_t *out_path,
+                                                           int32_t *out_count, int32_t *argmax_out,
+                                                           const float *logits, ts_tree t, int V, int seg,
+                                                           bool vec4, unsigned *counters, ArgPart *parts,
+                                                           uint32_t *status) {
+    const int b = blockIdx.y;
+    const int v = blockIdx.x / seg, sg = blockIdx.x % seg;
+    const int n = t.n_nodes[b];
+    const int n_max = t.n_max;
+    if (n <= 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) out_count[b] = 0;
+        return;
+    }
+    if (v >= n) return;
+    const float *row = logits + ((size_t)b * n_max + v) * V;
+    float bv = -FLT_MAX;
+    int bi = INT_MAX;
+    bool nf = false;
+    if (vec4) {
+        const int V4 = V >> 2, per = (V4 + seg - 1) / seg;
+        const int g0 = sg * per, g1 = min(V4, g0 + per);
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        int g = g0 + threadIdx.x;
+        for (; g + 3 * kGreedyThreads < g1; g += 4 * kGreedyThreads) {
+            float4 a[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) a[k] = __ldcs(r4 + g + k * kGreedyThreads);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = 4 * (g + k * kGreedyThreads);
+                // the four loads cover increasing indices only within one float4, so
+                // compare with the tie rule across them
+                float xs[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (!isfinite(xs[e])) nf = true;
+                    if (better(xs[e], i + e, bv, bi)) { bv = xs[e]; bi = i + e; }
+                }
+            }
+        }
+        for (; g < g1; g += kGreedyThreads) {
+            float4 a = __ldcs(r4 + g);
+            float xs[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!isfinite(xs[e])) nf = true;
+                if (better(xs[e], 4 * g + e, bv, bi)) { bv = xs[e]; bi = 4 * g + e; }
+            }
+        }
+    } else {
+        const int per = (V + seg - 1) / seg;
+        const int i0 = sg * per, i1 = min(V, i0 + per);
+        for (int i = i0 + threadIdx.x; i < i1; i += kGreedyThreads) consider(row[i], i, bv, bi, nf);
+    }
+    // block reduction of (value, index), lowest index on ties
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    nf = __any_sync(0xffffffffu, nf);
+    __shared__ float s_v[kGreedyThreads / 32];
+    __shared__ int s_i[kGreedyThreads / 32];
+    __shared__ int s_nf;
+    __shared__ bool s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) s_nf = 0;
+    __syncthreads();
+    if (lane == 0) {
+        s_v[warp] = bv;
+        s_i[warp] = bi;
+        if (nf) s_nf = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kGreedyThreads / 32; ++w)
+            if (better(s_v[w], s_i[w], bv, bi)) { bv = s_v[w]; bi = s_i[w]; }
+        ArgPart p;
+        p.val = bv;
+        p.idx = s_nf ? -1 : bi;
+        parts[((size_t)b * n_max + v) * seg + sg] = p;
+        __threadfence();
+        unsigned prev = atomicAdd(&counters[b], 1u);
+        s_last = prev == (unsigned)(n * seg - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    // ---- last CTA of request b: merge segments, then walk (Algorithm 2, VerifyGreedy)
+    __threadfence();
+    __shared__ int am[kMaxNodes];
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int w = threadIdx.x; w < n; w += kGreedyThreads) {
+        float cv = -FLT_MAX;
+        int ci = INT_MAX;
+        bool bad = false;
+        for (int k = 0; k < seg; ++k) {
+            const ArgPart *pp = parts + ((size_t)b * n_max + w) * seg + k;
+            float pv = __ldcg(&pp->val);
+            int pi = __ldcg(&pp->idx);
+            if (pi < 0) bad = true;
+            else if (better(pv, pi, cv, ci)) { cv = pv; ci = pi; }
+        }
+        am[w] = bad ? -1 : ci;
+        if (bad) s_bad = 1;
+        if (argmax_out) argmax_out[(size_t)b * n_max + w] = am[w];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        counters[b] = 0u;   // leave the workspace zeroed for the next call
+        int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
+        int32_t *op = out_path + (size_t)b * (n_max + 1);
+        const int32_t *perm = t.perm + (size_t)b * n_max;
+        const int32_t *tok = t.token + (size_t)b * n_max;
+        const int32_t *se = t.sub_end + (size_t)b * n_max;
+        if (s_bad) {
+            out_count[b] = 0;
+            flag(status, TS_STATUS_NONFINITE);
+        } else {
+            int u = 0, cnt = 0;
+            op[0] = perm[0];
+            for (int step = 0; step < n; ++step) {
+                const int o = am[perm[u]];
+                int next = -1;
+                for (int c = u + 1; c < se[u]; c = se[c])
+                    if (tok[c] == o) { next = c; break; }
+                ot[cnt++] = o;
+                if (next < 0) break;
+                op[cnt] = perm[next];
+                u = next;
+            }
+            out_count[b] = cnt;
+        }
+    }
+}
+
+// ------------------------------------------------------------------- MSS ----
+constexpr int kMssThreads = 1024;
+constexpr int kMssWarps = kMssThreads / 32;
+
+// float-float accumulation (Knuth two-sum)
+__device__ __forceinline__ void ff_add(float &hi, float &lo, float bh, float bl) {
+    float s = hi + bh;
+    float v = s - hi;
+    float e = (hi - (s - v)) + (bh - v);
+    e += lo + bl;
+    hi = s + e;
+    lo = e - (hi - s);
+}
+
+__device__ __forceinline__ void kahan(float &sum, float &comp, float x) {
+    float y = x - comp;
+    float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+}
+
+struct MssShared {
+    double red_d[kMssWarps];
+    float red_f[kMssWarps];
+    int red_i[kMssWarps];
+    double seg[kMssThreads];
+    int perm[kMaxNodes];
+    int tok[kMaxNodes];
+    int sub_end[kMaxNodes];
+    int prow[kMaxNodes];
+    int qrow[kMaxNodes];
+    const float *rej_q[kMaxNodes];
+    float rej_S[kMaxNodes];
+    double bcast_d;
+    float bcast_f;
+    int bcast_i;
+    int pick;
+};
+
+// Residual value at y: R_0 = e(y) / Z, R_{j+1} = max(0, R_j - S_j q_j(y)).
+// The scalar acceptance test and every vector pass use this same function.
+__device__ __forceinline__ float resid_at(const float *row, const float *const *rq, const float *rS, int nrej,
+                                          int y, float invT, float m, float invZ) {
+    float r = expf(__fmaf_rn(__ldg(row + y), invT, -m)) * invZ;
+    for (int j = 0; j < nrej; ++j) r = fmaxf(0.f, __fmaf_rn(-rS[j], __ldg(rq[j] + y), r));
+    return r;
+}
+
+__device__ double block_sum(MssShared &sm, float hi, float lo) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float bh = __shfl_xor_sync(0xffffffffu, hi, o);
+        float bl = __shfl_xor_sync(0xffffffffu, lo, o);
+        ff_add(hi, lo, bh, bl);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sm.red_d[warp] = (double)hi + (double)lo;
+    __syncthreads();
+    if (warp == 0) {
+        double x = sm.red_d[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) sm.bcast_d = x;
+    }
+    __syncthreads();
+    double r = sm.bcast_d;
+    __syncthreads();
+    return r;
+}
+
+__device__ float block_max(MssShared &sm, float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sm.red_f[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        float y = sm.red_f[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) y = fmaxf(y, __shfl_xor_sync(0xffffffffu, y, o));
+        if (lane == 0) sm.bcast_f = y;
+    }
+    __syncthreads();
+    float r = sm.bcast_f;
+    __syncthreads();
+    return r;
+}
+
+__device__ int block_or(MssShared &sm, int x) {
+    x = __any_sync(0xffffffffu, x);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sm.red_i[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int y = __any_sync(0xffffffffu, sm.red_i[lane]);
+        if (lane == 0) sm.bcast_i = y;
+    }
+    __syncthreads();
+    int r = sm.bcast_i;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+                                                        const float *logits, const int32_t *p_row, int NP,
+                                                        const float *ssm, const int32_t *q_row, int NQ,
+                                                        const float *uniforms, float invT, ts_tree t, int V,
+                                                        uint32_t *status) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    MssShared &sm = *reinterpret_cast<MssShared *>(smem_raw);
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int n = t.n_nodes[b];
+    const int n_max = t.n_max;
+    int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
+    int32_t *op = out_path + (size_t)b * (n_max + 1);
+    if (n <= 0) {
+        if (tid == 0) out_count[b] = 0;
+        return;
+    }
+    // tree and row indices into shared memory; index checks for every node
+    int bad_index = 0;
+    for (int i = tid; i < n; i += kMssThreads) {
+        const size_t o = (size_t)b * n_max + i;
+        const int v = t.perm[o];
+        sm.perm[i] = v;
+        sm.tok[i] = t.token[o];
+        sm.sub_end[i] = t.sub_end[o];
+        const int pr = p_row ? p_row[(size_t)b * n_max + v] : v;
+        sm.prow[i] = pr;
+        if (pr < 0 || pr >= NP) bad_index = 1;
+        if (i > 0) {
+            const int qr = q_row[(size_t)b * n_max + v];
+            sm.qrow[i] = qr;
+            if (qr < 0 || qr >= NQ || sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
+        }
+    }
+    __syncthreads();
+    if (block_or(sm, bad_index)) {
+        if (tid == 0) {
+            out_count[b] = 0;
+            flag(status, TS_STATUS_INDEX);
+        }
+        return;
+    }
+    const float *u_acc = uniforms + (size_t)b * 2 * n_max;
+    const float *u_smp = u_acc + n_max;
+    const bool vec = (V & 3) == 0;
+    const int V4 = V >> 2;
+    int u = 0, cnt = 0, nonfinite = 0;
+    if (tid == 0) op[0] = sm.perm[0];
+
+    for (int step = 0; step < n; ++step) {
+        const float *row = logits + ((size_t)b * NP + sm.prow[u]) * V;
+        // pass 1: max of the tempered logits, finiteness
+        float mx = -FLT_MAX;
+        int nf = 0;
+        if (vec) {
+            const float4 *r4 = reinterpret_cast<const float4 *>(row);
+            for (int g = tid; g < V4; g += kMssThreads) {
+                float4 a = __ldg(r4 + g);
+                nf |= !isfinite(a.x) | !isfinite(a.y) | !isfinite(a.z) | !isfinite(a.w);
+                mx = fmaxf(mx, fmaxf(fmaxf(a.x * invT, a.y * invT), fmaxf(a.z * invT, a.w * invT)));
+            }
+        } else {
+            for (int y = tid; y < V; y += kMssThreads) {
+                float a = __ldg(row + y);
+                nf |= !isfinite(a);
+                mx = fmaxf(mx, a * invT);
+            }
+        }
+        if (block_or(sm, nf)) { nonfinite = 1; break; }
+        const float m = block_max(sm, mx);
+        // pass 2: Z = sum exp(l/T - m)
+        float hi = 0.f, lo = 0.f;
+        {
+            float s = 0.f, c = 0.f;
+            if (vec) {
+                const float4 *r4 = reinterpret_cast<const float4 *>(row);
+                for (int g = tid; g < V4; g += kMssThreads) {
+                    float4 a = __ldg(r4 + g);
+                    kahan(s, c, expf(__fmaf_rn(a.x, invT, -m)));
+                    kahan(s, c, expf(__fmaf_rn(a.y, invT, -m)));
+                    kahan(s, c, expf(__fmaf_rn(a.z, invT, -m)));
+                    kahan(s, c, expf(__fmaf_rn(a.w, invT, -m)));
+                }
+            } else {
+                for (int y = tid; y < V; y += kMssThreads) kahan(s, c, expf(__fmaf_rn(__ldg(row + y), invT, -m)));
+            }
+            hi = s;
+            lo = -c;
+        }
+        const double Z = block_sum(sm, hi, lo);
+        const float invZ = (float)(1.0 / Z);
+
+        // children in input order: u+1, sub_end[u+1], ... below sub_end[u]
+        int nrej = 0;
+        double S = 1.0;
+        int accepted = -1;
+        for (int c = u + 1; c < sm.sub_end[u]; c = sm.sub_end[c]) {
+            const float *qc = ssm + ((size_t)b * NQ + sm.qrow[c]) * V;
+            const int x = sm.tok[c];
+            if (tid == 0) {
+                const float qx = __ldg(qc + x);
+                int acc = 0, bad = !isfinite(qx);
+                if (!bad) {
+                    double a = 1.0;
+                    if (qx > 0.f) {
+                        const float rx = resid_at(row, sm.rej_q, sm.rej_S, nrej, x, invT, m, invZ);
+                        a = fmin(1.0, (double)rx / (S * (double)qx));
+                    }
+                    acc = (double)u_acc[sm.perm[c]] <= a;
+                }
+                sm.pick = bad ? -2 : acc;
+            }
+            __syncthreads();
+            const int verdict = sm.pick;
+            __syncthreads();
+            if (verdict == -2) { nonfinite = 1; break; }
+            if (verdict == 1) { accepted = c; break; }
+            // rejection: S' = sum_y max(0, R(y) - S q_c(y))
+            const float Sf = (float)S;
+            float s = 0.f, cc = 0.f;
+            int bad = 0;
+            for (int y = tid; y < V; y += kMssThreads) {
+                const float qy = __ldg(qc + y);
+                bad |= !isfinite(qy);
+                const float r = resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ);
+                kahan(s, cc, fmaxf(0.f, __fmaf_rn(-Sf, qy, r)));
+            }
+            if (block_or(sm, bad)) { nonfinite = 1; break; }
+            const double Snew = block_sum(sm, s, -cc);
+            if (Snew > 0.0) {
+                if (tid == 0) {
+                    sm.rej_q[nrej] = qc;
+                    sm.rej_S[nrej] = Sf;
+                }
+                __syncthreads();
+                ++nrej;
+                S = Snew;
+            } else if (tid == 0) {
+                flag(status, TS_STATUS_ZERO_RESID);   // keep the residual unchanged
+            }
+        }
+        if (nonfinite) break;
+        if (accepted >= 0) {
+            if (tid == 0) {
+                ot[cnt] = sm.tok[accepted];
+                op[cnt + 1] = sm.perm[accepted];
+            }
+            ++cnt;
+            u = accepted;
+            continue;
+        }
+        // inverse CDF of the residual: contiguous segments per thread, fp64 scan
+        const int per = vec ? (V4 + kMssThreads - 1) / kMssThreads : (V + kMssThreads - 1) / kMssThreads;
+        const int unit = vec ? 4 : 1;
+        const int y0 = tid * per * unit, y1 = min(V, y0 + per * unit);
+        {
+            float s = 0.f, cc = 0.f;
+            for (int y = y0; y < y1; ++y) kahan(s, cc, resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ));
+            sm.seg[tid] = (double)s - (double)cc;
+        }
+        __syncthreads();
+        if (tid < 32) {     // exclusive scan of 1024 segment sums in fp64 by warp 0
+            double run = 0.0;
+            for (int k = 0; k < 32; ++k) run += sm.seg[tid * 32 + k];
+            double incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                double up = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += up;
+            }
+            double base = incl - run;
+            for (int k = 0; k < 32; ++k) {
+                double val = sm.seg[tid * 32 + k];
+                sm.seg[tid * 32 + k] = base;   // now the exclusive prefix
+                base += val;
+                if (k == 31 && tid == 31) sm.bcast_d = base;   // total
+            }
+        }
+        if (tid == 0) sm.pick = INT_MAX;
+        __syncthreads();
+        const double total = sm.bcast_d;
+        const double target = (double)u_smp[sm.perm[u]] * total;
+        {
+            const double lo_c = sm.seg[tid];
+            const double hi_c = tid + 1 < kMssThreads ? sm.seg[tid + 1] : total;
+            if (hi_c > lo_c && lo_c <= target && target < hi_c) atomicMin(&sm.pick, tid);
+        }
+        __syncthreads();
+        if (sm.pick == INT_MAX) {   // rounding left no bracket: the last segment with mass
+            if (tid == 0) sm.pick = -1;
+            __syncthreads();
+            const double lo_c = sm.seg[tid];
+            const double hi_c = tid + 1 < kMssThreads ? sm.seg[tid + 1] : total;
+            if (hi_c > lo_c) atomicMax(&sm.pick, tid);
+            __syncthreads();
+        }
+        if (tid == sm.pick || (sm.pick < 0 && tid == 0)) {
+            int chosen = -1, last_pos = -1;
+            if (sm.pick >= 0) {
+                double cum = sm.seg[tid];
+                for (int y = y0; y < y1; ++y) {
+                    const float r = resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ);
+                    cum += (double)r;
+                    if (r > 0.f) last_pos = y;
+                    if (r > 0.f && cum > target) { chosen = y; break; }
+                }
+            }
+            if (chosen < 0) chosen = last_pos >= 0 ? last_pos : 0;
+            ot[cnt] = chosen;
+        }
+        ++cnt;
+        break;
+    }
+    if (tid == 0) {
+        if (nonfinite) {
+            out_count[b] = 0;
+            flag(status, TS_STATUS_NONFINITE);
+        } else {
+            out_count[b] = cnt;
+        }
+    }
+}
+
+}  // namespace
+
+size_t greedy_ws_bytes(int B, int n_max, int V) {
+    (void)V;
+    size_t counters = ((size_t)B * sizeof(unsigned) + 255) / 256 * 256;
+    return counters + (size_t)B * n_max * kMaxSeg * sizeof(ArgPart);
+}
+
+cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *argmax_out,
+                                 const float *logits, const ts_tree &t, int V, void *ws, uint32_t *status,
+                                 cudaStream_t s) {
+    const int rows = t.B * t.n_max;
+    int seg = (4 * num_sms() + rows - 1) / rows;
+    seg = max(1, min(kMaxSeg, min(seg, V / 2048 > 0 ? V / 2048 : 1)));
+    const bool vec4 = (V % 4 == 0) && ((uintptr_t)logits % 16 == 0);
+    unsigned *counters = (unsigned *)ws;
+    ArgPart *parts = (ArgPart *)((char *)ws + ((size_t)t.B * sizeof(unsigned) + 255) / 256 * 256);
+    dim3 grid(t.n_max * seg, t.B);
+    k_greedy<<<grid, kGreedyThreads, 0, s>>>(out_tokens, out_path, out_count, argmax_out, logits, t, V, seg, vec4,
+                                             counters, parts, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
+                              const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
+                              const float *uniforms, float temperature, const ts_tree &t, int V,
+                              uint32_t *status, cudaStream_t s) {
+    const size_t smem = sizeof(MssShared);   // below the 48 KB default limit
+    const bool vec = (V % 4 == 0) && ((uintptr_t)logits % 16 == 0);
+    if (!vec && V % 4 == 0) return cudaErrorMisalignedAddress;
+    k_mss<<<t.B, kMssThreads, smem, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row, NQ,
+                                         uniforms, 1.0f / temperature, t, V, status);
+    return cudaGetLastError();
+}
+
+}  // namespace ts

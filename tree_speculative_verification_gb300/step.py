@@ -1,0 +1,117 @@
+"""One tree-verification step on the GPU, driven through the C ABI.
+
+DeviceStep holds a workload's tensors on the device (KV cache, Q / new K/V,
+logits, drafter probabilities, uniforms) and the output buffers, and runs the
+hot path: tree_build -> kv_append -> tree_attention -> verify (greedy and/or
+MSS) -> kv_commit. kv_commit writes the new prefix lengths into a separate
+array, so repeating a step on the same inputs is idempotent.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import api
+from .workloads import Workload
+
+
+def to_device(a: np.ndarray, device, bf16: bool = False) -> torch.Tensor:
+    if bf16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DeviceStep:
+    def __init__(self, w: Workload, device="cuda", attention: bool = True):
+        self.w = w
+        self.device = device
+        dev = device
+        B, n_max = w.B, w.n_max
+        i32 = lambda a: to_device(np.asarray(a, np.int32), dev)
+        self.tree = api.Tree(B, n_max, dev)
+        self.prefix_len = i32(w.prefix_len)
+        self.new_prefix_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.tree_mode == "chains":
+            self.chains = i32(w.chains)
+            self.root_token = i32(w.root_token)
+            self.tokens = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
+            self.p_row = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
+            self.q_row = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
+        else:
+            self.tokens = i32(w.tokens)
+            self.parent = i32(w.parent)
+            self.n_nodes_in = i32(w.n_nodes)
+            self.p_row = None
+            self.q_row = i32(w.q_row) if w.q_row is not None else None
+        self.logits = to_device(w.logits, dev)
+        self.ssm = to_device(w.ssm, dev) if w.ssm is not None else None
+        self.uniforms = to_device(w.uniforms, dev)
+        self.out_tokens = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
+        self.out_path = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
+        self.out_count = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.mss_tokens = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
+        self.mss_path = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
+        self.mss_count = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.argmax = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
+        self.ws_greedy = api.workspace(api.TS_OP_VERIFY_GREEDY, B, n_max=n_max, V=w.V, device=dev)
+        self.attention = attention and w.q is not None
+        if self.attention:
+            bf = w.dtype == "bf16"
+            self.q = to_device(w.q, dev, bf)
+            self.k_new = to_device(w.k_new, dev, bf)
+            self.v_new = to_device(w.v_new, dev, bf)
+            self.k_cache = to_device(w.k_cache, dev, bf)
+            self.v_cache = to_device(w.v_cache, dev, bf)
+            self.out = torch.zeros_like(self.q)
+            self.ws_attn = api.workspace(api.TS_OP_ATTENTION, B, w.H, n_max, w.d, w.L_max, w.V, device=dev)
+
+    # -- the five rows of the hot path ----------------------------------------
+    def build(self, stream=None):
+        w = self.w
+        if w.tree_mode == "chains":
+            api.tree_build_chains(self.tree, self.root_token, self.chains, self.tokens, self.p_row, self.q_row,
+                                  self.prefix_len, self.status, stream)
+        elif w.tree_mode == "widths":
+            api.tree_build(self.tree, self.tokens, widths=w.widths, prefix_len=self.prefix_len, status=self.status,
+                           stream=stream)
+        else:
+            api.tree_build(self.tree, self.tokens, self.parent, self.n_nodes_in, prefix_len=self.prefix_len,
+                           status=self.status, stream=stream)
+
+    def append(self, stream=None):
+        api.kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.prefix_len, self.tree, self.status,
+                      stream)
+
+    def attend(self, stream=None):
+        api.tree_attention(self.out, self.q, self.k_cache, self.v_cache, self.prefix_len, self.tree, 0.0,
+                           self.ws_attn, self.status, stream)
+
+    def verify(self, kind: str | None = None, stream=None):
+        kind = kind or self.w.verify
+        if kind in ("greedy", "both"):
+            api.verify_greedy(self.out_tokens, self.out_path, self.out_count, self.logits, self.tree, self.argmax,
+                              self.ws_greedy, self.status, stream)
+        if kind in ("mss", "both"):
+            api.verify_mss(self.mss_tokens, self.mss_path, self.mss_count, self.logits, self.ssm, self.q_row,
+                           self.uniforms, self.w.temperature, self.tree, p_row=self.p_row, status=self.status,
+                           stream=stream)
+
+    def commit(self, kind: str | None = None, stream=None):
+        kind = kind or self.w.verify
+        path, count = (self.mss_path, self.mss_count) if kind in ("mss", "both") else (self.out_path, self.out_count)
+        api.kv_commit(self.k_cache, self.v_cache, self.prefix_len, self.new_prefix_len, path, count, self.tree,
+                      self.status, stream)
+
+    def run(self, kind: str | None = None, stream=None):
+        self.build(stream)
+        if self.attention:
+            self.append(stream)
+            self.attend(stream)
+        self.verify(kind, stream)
+        if self.attention:
+            self.commit(kind, stream)
+
+    def launches_per_step(self, kind: str | None = None) -> int:
+        kind = kind or self.w.verify
+        return 1 + (3 if self.attention else 0) + (2 if kind == "both" else 1)
