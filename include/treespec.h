@@ -219,6 +219,35 @@ ts_status kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len,
                     const ts_tree *t, int H, int d, int L_max, ts_dtype dtype, uint32_t *status,
                     cudaStream_t stream);
 
+/*
+ * tree_attention_noalloc -- tree_attention for callers that cannot allocate
+ * device memory. The paper has no counterpart: this is a packaging variant of
+ * the same computation. Some callers may not call cudaMalloc themselves --
+ * plugin or callback code run by a host framework that owns every device
+ * allocation and forbids allocating on its execution path, or serving loops
+ * that must not allocate once warmed up. They pass inputs and outputs exactly
+ * as for tree_attention but no workspace: the split-KV partial results go to
+ * a scratch array of TS_NOALLOC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *  - Sizes whose workspace (treespec_workspace_size(TS_OP_ATTENTION, ...))
+ *    exceeds TS_NOALLOC_SCRATCH_BYTES are rejected with TS_ERR_INVALID_ARG
+ *    and a message saying so; nothing is launched.
+ *  - The first call on a device looks the scratch address up
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls on a device share the one scratch array, which keeps the last
+ *    call's contents; each call clears the part that must start at zero on
+ *    its stream (cudaMemsetAsync). Calls whose kernels may overlap on the GPU
+ *    (different streams with no ordering) race on the scratch and must not be
+ *    issued.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * fp32 inputs need no workspace and behave exactly as tree_attention.
+ */
+#define TS_NOALLOC_SCRATCH_BYTES (8u << 20)
+ts_status tree_attention_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max,
+                                 ts_dtype dtype, float scale, uint32_t *status, cudaStream_t stream);
+
 /* Bytes of workspace an op needs for these sizes on the current device (0 if none). */
 size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_max, int V);
 

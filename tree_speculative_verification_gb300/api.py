@@ -25,7 +25,9 @@ MAX_NODES = 256
 #: every entry point of the C ABI (include/treespec.h)
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
-           "treespec_version")
+           "treespec_version", "tree_attention_noalloc")
+#: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class TreespecError(RuntimeError):
@@ -62,6 +64,7 @@ def load_library(path: str | None = None):
         "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
         "kv_commit": [P, P, P, P, P, P, T, I, I, I, I, P, P],
         "treespec_workspace_init": [P, Z, P],
+        "tree_attention_noalloc": [P, P, P, P, P, T, I, I, I, I, F, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -179,6 +182,18 @@ def tree_attention(out, q, k_cache, v_cache, prefix_len, tree: Tree, scale: floa
     _check(lib.tree_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(_i32(prefix_len, "prefix_len")),
                               tree.c, H, d, L_max, _dtype(k_cache), float(scale), _ptr(ws), nbytes, _ptr(status),
                               _stream(stream)), "tree_attention")
+
+
+def tree_attention_noalloc(out, q, k_cache, v_cache, prefix_len, tree: Tree, scale: float = 0.0, status=None,
+                           stream=None):
+    """tree_attention without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in scratch array (shared by all
+    calls on a device; calls must not overlap on the GPU) holds the partials."""
+    lib = load_library()
+    B, H, L_max, d = k_cache.shape
+    _check(lib.tree_attention_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(_i32(prefix_len, "prefix_len")), tree.c, H, d, L_max, _dtype(k_cache),
+                                      float(scale), _ptr(status), _stream(stream)), "tree_attention_noalloc")
 
 
 def verify_greedy(out_tokens, out_path, out_count, logits, tree: Tree, argmax_out=None, ws=None, status=None,

@@ -53,6 +53,18 @@ ts_status check_attn_shape(const char *who, const ts_tree *t, int H, int d, int 
 
 }  // namespace
 
+namespace ts {
+// Records the message returned by treespec_last_error() for entry points
+// defined in other translation units.
+ts_status set_error(ts_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+}  // namespace ts
+
 extern "C" {
 
 const char *treespec_last_error(void) { return g_err; }

@@ -70,4 +70,6 @@ cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *o
 
 int num_sms();
 
+ts_status set_error(ts_status st, const char *fmt, ...);
+
 }  // namespace ts
