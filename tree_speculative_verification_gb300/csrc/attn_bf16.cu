@@ -51,7 +51,7 @@ struct Cfg {
     static constexpr int OFF_ANC = OFF_Q + Q_BYTES;
     static constexpr int OFF_PERM = OFF_ANC + ANC_BYTES;
     static constexpr int OFF_BAR = OFF_PERM + NODES * 4;
-    static constexpr int OFF_MISC = OFF_BAR + STAGES * 8;
+    static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack for 1024-byte alignment
     static_assert(NG * (KS - 1) * SLOT_FLOATS * 4 <= STAGES * STAGE_BYTES, "merge slots exceed stage memory");
     static_assert(KEYS_PER_WARP % 16 == 0, "warp key slice must be a multiple of 16");
@@ -78,6 +78,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
         : "r"(bar), "r"(phase)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Bounded wait: false after kWaitCycles without completion.
@@ -182,7 +186,10 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
     const uint32_t bar0 = sm_base + C::OFF_BAR;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8 * s, 1);                              // full: TMA bytes landed
+            mbar_init(bar0 + 8 * (STAGES + s), C::WARPS);            // empty: every warp done
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -254,18 +261,22 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
         l_run[j][0] = l_run[j][1] = 0.f;
     }
 
-    bool timed_out = false;
+    // Main loop. Stage st of the ring is refilled by thread 0 once every warp
+    // has released it (empty barrier, one arrival per warp), so warps are not
+    // coupled by a CTA-wide barrier per tile.
+    const uint32_t ebar0 = bar0 + 8 * STAGES;
+    const float c = a.scale_log2;
+    int timed_out = 0;
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % STAGES;
         const uint32_t phase = (uint32_t)(it / STAGES) & 1u;
-        timed_out = !mbar_wait_bounded(bar0 + 8 * st, phase);
-        if (__syncthreads_or(timed_out)) { timed_out = true; break; }
+        if (!mbar_wait_bounded(bar0 + 8 * st, phase)) { timed_out = 1; break; }
         const int key_base = k_begin + it * TK;
         unsigned char *ktile = sm + st * C::STAGE_BYTES;
         unsigned char *vtile = ktile + C::TILE_BYTES;
         if (key_base + TK > k_end) {
-            // rows past the chunk may hold anything (even NaN): zero their V so
-            // that a zero probability multiplies a zero
+            // last tile: rows past the chunk may hold anything (even NaN); zero
+            // their V so that a zero probability multiplies a zero
             for (int idx = tid; idx < TK * C::BOXES * 8; idx += C::THREADS) {
                 const int r = idx / (C::BOXES * 8), rem = idx % (C::BOXES * 8);
                 if (key_base + r >= k_end)
@@ -275,85 +286,90 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
         }
         const uint32_t kb_addr = smem_u32(ktile), vb_addr = smem_u32(vtile);
 #pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c) {
-            const int kb = ks * C::KEYS_PER_WARP + c * 16;
+        for (int ch16 = 0; ch16 < C::CHUNKS; ++ch16) {
+            const int kb = ks * C::KEYS_PER_WARP + ch16 * 16;
             const int key0 = key_base + kb;
             if (key0 >= k_end) break;
-            // S^T = K Q^T : 16 keys x (NT*8) nodes
+            // S^T = K Q^T : 16 keys x (NT*8) nodes, raw dot products
             float sacc[NT][4];
 #pragma unroll
             for (int j = 0; j < NT; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int r = kb + (lane & 7) + (((lane >> 3) & 1) << 3);
-                const int ch = 2 * (kk & 3) + (lane >> 4);
+                const int chn = 2 * (kk & 3) + (lane >> 4);
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(kb_addr + (kk >> 2) * C::BOX_BYTES + swz(r, ch), a0, a1, a2, a3);
+                ldsm_x4(kb_addr + (kk >> 2) * C::BOX_BYTES + swz(r, chn), a0, a1, a2, a3);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qf[j][kk][0], qf[j][kk][1]);
             }
-            // mask, scale, column max over the 16 keys
+            // the mask is needed only where the chunk reaches the tree rows or the chunk end
+            if (key0 + 16 > P || key0 + 16 > k_end) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + g + ((e >> 1) << 3);
+                        const int node = node0 + j * 8 + 2 * tq + (e & 1);
+                        bool vis = key < k_end;
+                        if (vis && key >= P) {
+                            const int tk = key - P;
+                            vis = (anc_s[node * kMaxWords + (tk >> 5)] >> (tk & 31)) & 1u;
+                        }
+                        if (!vis) sacc[j][e] = -INFINITY;
+                    }
+            }
+            // column max over the 16 keys (raw scores; the scale is positive)
             float cmax[NT][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = key0 + g + ((e >> 1) << 3);
-                    const int node = node0 + j * 8 + 2 * tq + (e & 1);
-                    bool vis = key < k_end;
-                    if (vis && key >= P) {
-                        const int tk = key - P;
-                        vis = (anc_s[node * kMaxWords + (tk >> 5)] >> (tk & 31)) & 1u;
-                    }
-                    sacc[j][e] = vis ? sacc[j][e] * a.scale_log2 : -INFINITY;
-                }
                 cmax[j][0] = fmaxf(sacc[j][0], sacc[j][2]);
                 cmax[j][1] = fmaxf(sacc[j][1], sacc[j][3]);
-            }
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     float v = cmax[j][x];
                     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
                     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
                     v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-                    cmax[j][x] = v;
+                    cmax[j][x] = v * c;
                 }
+            }
             // online rescale, only when some column's running max moved
             bool grow = false;
-            float alpha[NT][2], m_use[NT][2];
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const float mn = fmaxf(m_run[j][x], cmax[j][x]);
-                    alpha[j][x] = (mn == m_run[j][x]) ? 1.f : exp2f(m_run[j][x] - mn);
-                    grow |= mn != m_run[j][x];
-                    m_run[j][x] = mn;
-                    m_use[j][x] = mn == -INFINITY ? 0.f : mn;
-                }
+            for (int j = 0; j < NT; ++j) grow |= (cmax[j][0] > m_run[j][0]) | (cmax[j][1] > m_run[j][1]);
             if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    l_run[j][0] *= alpha[j][0];
-                    l_run[j][1] *= alpha[j][1];
+                    float al[2];
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const float mn = fmaxf(m_run[j][x], cmax[j][x]);
+                        al[x] = mn == m_run[j][x] ? 1.f : exp2f(m_run[j][x] - mn);
+                        m_run[j][x] = mn;
+                    }
+                    l_run[j][0] *= al[0];
+                    l_run[j][1] *= al[1];
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
-                        oacc[mt][j][0] *= alpha[j][0];
-                        oacc[mt][j][1] *= alpha[j][1];
-                        oacc[mt][j][2] *= alpha[j][0];
-                        oacc[mt][j][3] *= alpha[j][1];
+                        oacc[mt][j][0] *= al[0];
+                        oacc[mt][j][1] *= al[1];
+                        oacc[mt][j][2] *= al[0];
+                        oacc[mt][j][3] *= al[1];
                     }
                 }
             }
-            // P^T (bf16) in the B-operand layout
+            // P^T (bf16) in the B-operand layout; p = exp2(s * c - m)
             uint32_t pb[NT][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
+                const float mu0 = m_run[j][0] == -INFINITY ? 0.f : m_run[j][0];
+                const float mu1 = m_run[j][1] == -INFINITY ? 0.f : m_run[j][1];
                 float r0, r1, r2, r3;
-                const uint32_t x0 = pack_bf16(exp2f(sacc[j][0] - m_use[j][0]), exp2f(sacc[j][1] - m_use[j][1]), r0, r1);
-                const uint32_t x1 = pack_bf16(exp2f(sacc[j][2] - m_use[j][0]), exp2f(sacc[j][3] - m_use[j][1]), r2, r3);
+                const uint32_t x0 = pack_bf16(exp2f(__fmaf_rn(sacc[j][0], c, -mu0)),
+                                              exp2f(__fmaf_rn(sacc[j][1], c, -mu1)), r0, r1);
+                const uint32_t x1 = pack_bf16(exp2f(__fmaf_rn(sacc[j][2], c, -mu0)),
+                                              exp2f(__fmaf_rn(sacc[j][3], c, -mu1)), r2, r3);
                 l_run[j][0] += r0 + r2;
                 l_run[j][1] += r1 + r3;
                 pb[j][0] = movm_t(x0);
@@ -363,17 +379,21 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
                 const int r = kb + (lane & 7) + ((lane >> 4) << 3);
-                const int ch = 2 * (mt & 3) + ((lane >> 3) & 1);
+                const int chn = 2 * (mt & 3) + ((lane >> 3) & 1);
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(vb_addr + (mt >> 2) * C::BOX_BYTES + swz(r, ch), a0, a1, a2, a3);
+                ldsm_x4_t(vb_addr + (mt >> 2) * C::BOX_BYTES + swz(r, chn), a0, a1, a2, a3);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) mma_bf16(oacc[mt][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
             }
         }
-        __syncthreads();   // every warp is done with this stage
-        if (tid == 0 && it + STAGES < ntiles) issue(it + STAGES);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ebar0 + 8 * st);
+        if (tid == 0 && it + STAGES < ntiles) {
+            if (!mbar_wait_bounded(ebar0 + 8 * st, phase)) { timed_out = 1; break; }
+            issue(it + STAGES);
+        }
     }
-    if (timed_out) {   // uniform: decided by __syncthreads_or above
+    if (__syncthreads_or(timed_out)) {
         if (tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
         return;
     }
