@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
+#include <string.h>
 
 #include "ts_internal.cuh"
 
@@ -153,6 +154,44 @@ struct AttnArgs {
     float *part_o;    // [B*H*splits][n_pad][D]
     uint32_t *status;
 };
+
+// After a CTA has published its partial (max, sum, unnormalised O) for key
+// split sidx of (b, h), the CTA that arrives last on the (b, h) counter merges
+// all S_b partials by log-sum-exp and writes the bf16 rows. No CTA waits: the
+// others return. Called by every thread of the CTA.
+template <int D>
+__device__ void merge_splits(const AttnArgs &a, int b, int h, int n, int S_b, const int *perm_s, int *flag_s,
+                             int nthreads) {
+    const int tid = threadIdx.x;
+    const size_t bh = (size_t)b * a.H + h;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) flag_s[0] = atomicAdd(&a.counters[bh], 1u) == (unsigned)(S_b - 1);
+    __syncthreads();
+    if (!flag_s[0]) return;
+    __threadfence();
+    const int n_max = a.t.n_max;
+    for (int idx = tid; idx < n * (D / 2); idx += nthreads) {
+        const int i = idx / (D / 2), dp = (idx % (D / 2)) * 2;
+        float M = -INFINITY;
+        for (int s = 0; s < S_b; ++s) M = fmaxf(M, __ldcg(a.part_ml + (bh * a.splits + s) * 2 * a.n_pad + i));
+        float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+        for (int s = 0; s < S_b; ++s) {
+            const float *pml = a.part_ml + (bh * a.splits + s) * 2 * a.n_pad;
+            const float ms = __ldcg(pml + i);
+            if (ms == -INFINITY) continue;
+            const float f = exp2f(ms - M);
+            Lsum += __ldcg(pml + a.n_pad + i) * f;
+            const float2 ov = __ldcg((const float2 *)(a.part_o + ((bh * a.splits + s) * a.n_pad + i) * D + dp));
+            o0 += ov.x * f;
+            o1 += ov.y * f;
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        *(__nv_bfloat162 *)(a.out + (((size_t)b * n_max + perm_s[i]) * a.H + h) * D + dp) =
+            __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    }
+    if (tid == 0) a.counters[bh] = 0u;   // leave the workspace zeroed
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant__ CUtensorMap map_k,
@@ -516,32 +555,380 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
             }
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) misc[0] = atomicAdd(&a.counters[bh], 1u) == (unsigned)(S_b - 1);
-    __syncthreads();
-    if (!misc[0]) return;
-    __threadfence();
-    for (int idx = tid; idx < n * (D / 2); idx += C::THREADS) {
-        const int i = idx / (D / 2), dp = (idx % (D / 2)) * 2;
-        float M = -INFINITY;
-        for (int s = 0; s < S_b; ++s) M = fmaxf(M, __ldcg(a.part_ml + (bh * a.splits + s) * 2 * a.n_pad + i));
-        float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
-        for (int s = 0; s < S_b; ++s) {
-            const float *pml = a.part_ml + (bh * a.splits + s) * 2 * a.n_pad;
-            const float ms = __ldcg(pml + i);
-            if (ms == -INFINITY) continue;
-            const float f = exp2f(ms - M);
-            Lsum += __ldcg(pml + a.n_pad + i) * f;
-            const float2 ov = __ldcg((const float2 *)(a.part_o + ((bh * a.splits + s) * a.n_pad + i) * D + dp));
-            o0 += ov.x * f;
-            o1 += ov.y * f;
-        }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        *(__nv_bfloat162 *)(a.out + (((size_t)b * n_max + perm_s[i]) * a.H + h) * D + dp) =
-            __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    merge_splits<D>(a, b, h, n, S_b, perm_s, misc, C::THREADS);
+}
+
+
+// ============================================================================
+// tcgen05 variant (trees of up to 128 nodes, head_dim 128).
+//
+// One CTA of 6 warps per (request, head, key chunk):
+//   warp 0    TMA producer (lane 0) and TMEM owner (alloc / dealloc)
+//   warp 1    MMA issuer (lane 0): S = Q K^T and O += P V with tcgen05.mma
+//   warps 2-5 softmax: thread r of TMEM lane quarter (warp % 4) owns node row
+//             r, reads its score row from TMEM, masks it, keeps a running max
+//             (rescaling O in TMEM only when the max grows by more than 2^8),
+//             writes bf16 P to shared memory.
+// Per 64-key tile: S (M = 128 node rows, N = 64 keys, K = 128) lands in one
+// of two TMEM score buffers; O (M = 128, N = 128, K = 64 keys) accumulates in
+// TMEM. Q, K and P are K-major, V is MN-major, all in the 128-byte swizzled
+// layout TMA writes. Every wait is bounded.
+// ============================================================================
+struct TcCfg {
+    static constexpr int D = 128, TKT = 64, STAGES = 4, NODES = 128, THREADS = 192;
+    static constexpr int BOX_BYTES = TKT * 128;           // 64 key rows x 128 bytes
+    static constexpr int TILE_BYTES = 2 * BOX_BYTES;      // K (or V) of 64 keys x 128 dims
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
+    static constexpr int QBOX = NODES * 128;              // 128 node rows x 64 dims
+    static constexpr int Q_BYTES = 2 * QBOX;
+    static constexpr int P_BYTES = NODES * 128;           // 128 node rows x 64 keys
+    static constexpr int ANC_WORDS = 4;                   // 128 nodes
+    static constexpr int OFF_Q = STAGES * STAGE_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;
+    static constexpr int OFF_ANC = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_PERM = OFF_ANC + NODES * ANC_WORDS * 4;
+    static constexpr int NBAR = 2 * STAGES + 2 * 4 + 1;   // full, empty, s_full, s_free, p_full, pv_done, fin
+    static constexpr int OFF_BAR = OFF_PERM + NODES * 4;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static constexpr uint32_t TMEM_COLS = 256;            // S0 [0,64), S1 [64,128), O [128,256)
+};
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version of the sm_100 family
+    d |= (uint64_t)2 << 61;   // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, A K-major.
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_constant__ CUtensorMap map_k,
+                                                               const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+    using C = TcCfg;
+    constexpr int D = C::D;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sm_base = smem_u32(sm);
+    uint32_t *anc_s = (uint32_t *)(sm + C::OFF_ANC);
+    int *perm_s = (int *)(sm + C::OFF_PERM);
+    volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout, [2] merge flag
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
+    const ts_tree &t = a.t;
+    const int n = t.n_nodes[b], P = a.prefix_len[b];
+    if (n <= 0) return;
+    if (P < 0 || P + n > a.L_max) {
+        if (sidx == 0 && h == 0 && tid == 0) flag(a.status, TS_STATUS_INDEX);
+        return;
     }
-    if (tid == 0) a.counters[bh] = 0u;   // leave the workspace zeroed
+    const int L = P + n;
+    const int chunk_keys = a.chunk_tiles * TK;   // the plan counts 64-key tiles
+    const int S_b = (L + chunk_keys - 1) / chunk_keys;
+    if (sidx >= S_b) return;
+    const int k_begin = sidx * chunk_keys, k_end = min(L, k_begin + chunk_keys);
+    const int ntiles = (k_end - k_begin + C::TKT - 1) / C::TKT;
+    const int row0 = (b * a.H + h) * a.L_max + k_begin;
+
+    const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
+    const uint32_t s_full = empty + 8 * C::STAGES, s_free = s_full + 16, p_full = s_free + 16, pv_done = p_full + 16;
+    const uint32_t fin = pv_done + 16;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 32) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full + 8 * x, 1);
+            mbar_init(s_free + 8 * x, 4);
+            mbar_init(p_full + 8 * x, 4);
+            mbar_init(pv_done + 8 * x, 1);
+        }
+        mbar_init(fin, 1);
+        misc[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // Q rows (DFS order) in the 128-byte swizzled K-major layout; zero rows past n
+    const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
+    for (int r = tid; r < C::NODES; r += C::THREADS) perm_s[r] = r < n ? t.perm[(size_t)b * n_max + r] : -1;
+    __syncthreads();
+    for (int idx = tid; idx < C::NODES * 16; idx += C::THREADS) {
+        const int r = idx >> 4, c = idx & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n) val = ((const uint4 *)(a.q + (((size_t)b * n_max + perm_s[r]) * a.H + h) * D))[c];
+        *(uint4 *)(sm + C::OFF_Q + (c >> 3) * C::QBOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val;
+    }
+    for (int idx = tid; idx < C::NODES * C::ANC_WORDS; idx += C::THREADS) {
+        const int r = idx / C::ANC_WORDS, w = idx % C::ANC_WORDS;
+        anc_s[idx] = (r < n && w < W) ? t.anc[((size_t)b * n_max + r) * W + w] : 0u;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------------------------------------- TMA producer
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % C::STAGES;
+                if (j >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((j / C::STAGES) - 1) & 1u)) {
+                    misc[1] = 1;
+                    break;
+                }
+                const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
+                mbar_expect_tx(full + 8 * st, C::STAGE_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row0 + j * C::TKT, full + 8 * st);
+                    tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row0 + j * C::TKT, full + 8 * st);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------------------------------------- MMA issuer
+            constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+            const uint32_t q_base = sm_base + C::OFF_Q;
+            for (int j = 0; j <= ntiles && !misc[1]; ++j) {
+                if (j < ntiles) {
+                    const int st = j % C::STAGES;
+                    if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u) ||
+                        (j >= 2 && !mbar_wait_bounded(s_free + 8 * (j & 1), (uint32_t)((j >> 1) - 1) & 1u))) {
+                        misc[1] = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(q_base + (kk >> 2) * C::QBOX + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                        tc_mma(tmem + (j & 1) * C::TKT, ad, bd, idesc_s, kk > 0);
+                    }
+                    tc_commit(s_full + 8 * (j & 1));
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, st2 = jj % C::STAGES;
+                    if (!mbar_wait_bounded(p_full + 8 * (jj & 1), (uint32_t)(jj >> 1) & 1u)) {
+                        misc[1] = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pbase = sm_base + C::OFF_P + (jj & 1) * C::P_BYTES;
+                    const uint32_t vbase = sm_base + st2 * C::STAGE_BYTES + C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < C::TKT / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
+                        tc_mma(tmem + 2 * C::TKT, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty + 8 * st2);
+                    tc_commit(pv_done + 8 * (jj & 1));
+                }
+            }
+            tc_commit(fin);   // completes once every MMA issued above has finished
+            if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
+        }
+    } else {   // --------------------------------------------------------- softmax
+        const int wq = warp & 3, row = wq * 32 + lane;
+        const bool active = wq * 32 < n;
+        const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+        uint32_t aw[C::ANC_WORDS];
+#pragma unroll
+        for (int w = 0; w < C::ANC_WORDS; ++w) aw[w] = anc_s[row * C::ANC_WORDS + w];
+        const float c = a.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int sb = j & 1;
+            if (!mbar_wait_bounded(s_full + 8 * sb, (uint32_t)(j >> 1) & 1u)) { ok = false; break; }
+            tc_fence_after();
+            float sv[64];
+            if (active) {
+                tc_ld32(tl + sb * C::TKT, *reinterpret_cast<float(*)[32]>(&sv[0]));
+                tc_ld32(tl + sb * C::TKT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+                tc_wait_ld();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free + 8 * sb);
+            uint32_t pk[32];
+            if (active) {
+                const int key_base = k_begin + j * C::TKT;
+                if (key_base + C::TKT > P || key_base + C::TKT > k_end) {
+#pragma unroll
+                    for (int k = 0; k < C::TKT; ++k) {
+                        const int key = key_base + k;
+                        bool vis = key < k_end;
+                        if (vis && key >= P) {
+                            const int tk = key - P;
+                            vis = (aw[tk >> 5] >> (tk & 31)) & 1u;
+                        }
+                        if (!vis) sv[k] = -INFINITY;
+                    }
+                }
+                float mt = sv[0];
+#pragma unroll
+                for (int k = 1; k < C::TKT; ++k) mt = fmaxf(mt, sv[k]);
+                mt *= c;
+                float alpha = 1.f;
+                bool resc = false;
+                if (m_run == -INFINITY) {
+                    m_run = mt;                              // nothing accumulated yet for this row
+                } else if (mt > m_run + 8.f) {
+                    alpha = exp2f(m_run - mt);
+                    m_run = mt;
+                    resc = true;
+                }
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O must hold every earlier tile before it is rescaled
+                    if (j >= 1 && !mbar_wait_bounded(pv_done + 8 * ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u)) {
+                        ok = false;
+                    } else {
+                        tc_fence_after();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float o[32];
+                            tc_ld32(tl + 2 * C::TKT + q4 * 32, o);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                            tc_st32(tl + 2 * C::TKT + q4 * 32, o);
+                        }
+                        tc_wait_st();
+                        l_run *= alpha;
+                    }
+                }
+                const float mu = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+                for (int k = 0; k < C::TKT; k += 2) {
+                    float r0, r1;
+                    pk[k >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[k], c, -mu)), exp2f(__fmaf_rn(sv[k + 1], c, -mu)), r0, r1);
+                    l_run += r0 + r1;
+                }
+            }
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            {
+                // last tile: V rows past the chunk may hold anything (even NaN);
+                // zero them before the PV reads the stage, so 0 * V stays 0
+                const int key_base = k_begin + j * C::TKT;
+                if (key_base + C::TKT > k_end) {
+                    const int st = j % C::STAGES;
+                    if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) { ok = false; break; }
+                    unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
+                    const int r0 = k_end - key_base;
+                    for (int idx = tid - 64; idx < (C::TKT - r0) * 16; idx += 128) {
+                        const int r = r0 + (idx >> 4), c16 = idx & 15;
+                        *(uint4 *)(vt + (c16 >> 3) * C::BOX_BYTES + r * 128 + ((c16 & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_async_smem();
+                }
+            }
+            // the P buffer of tile j was read by the PV of tile j - 2
+            if (j >= 2 && !mbar_wait_bounded(pv_done + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u)) { ok = false; break; }
+            if (active) {
+                unsigned char *prow = sm + C::OFF_P + sb * C::P_BYTES + row * 128;
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16)
+                    *(uint4 *)(prow + ((c16 ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+                fence_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + 8 * sb);
+        }
+        if (!ok) misc[1] = 1;
+        // O is complete once the last PV has finished
+        if (ok && mbar_wait_bounded(pv_done + 8 * ((ntiles - 1) & 1), (uint32_t)((ntiles - 1) >> 1) & 1u)) {
+            tc_fence_after();
+            if (active) {
+                float o[D];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tc_ld32(tl + 2 * C::TKT + q4 * 32, *reinterpret_cast<float(*)[32]>(&o[q4 * 32]));
+                tc_wait_ld();
+                if (row < n) {
+                    if (S_b == 1) {
+                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                        uint4 *dst = (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D);
+#pragma unroll
+                        for (int c16 = 0; c16 < D / 8; ++c16) {
+                            float dummy0, dummy1;
+                            uint4 v;
+                            v.x = pack_bf16(o[8 * c16] * inv, o[8 * c16 + 1] * inv, dummy0, dummy1);
+                            v.y = pack_bf16(o[8 * c16 + 2] * inv, o[8 * c16 + 3] * inv, dummy0, dummy1);
+                            v.z = pack_bf16(o[8 * c16 + 4] * inv, o[8 * c16 + 5] * inv, dummy0, dummy1);
+                            v.w = pack_bf16(o[8 * c16 + 6] * inv, o[8 * c16 + 7] * inv, dummy0, dummy1);
+                            dst[c16] = v;
+                        }
+                    } else {
+                        const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
+                        a.part_ml[ps * 2 * a.n_pad + row] = m_run;
+                        a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = l_run;
+                        float4 *po = (float4 *)(a.part_o + (ps * a.n_pad + row) * D);
+#pragma unroll
+                        for (int c4 = 0; c4 < D / 4; ++c4) po[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+                    }
+                }
+            }
+        } else {
+            misc[1] = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    if (misc[1]) {
+        if (tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
+        return;
+    }
+    if (S_b > 1) merge_splits<D>(a, b, h, n, S_b, perm_s, (int *)misc + 2, C::THREADS);
 }
 
 // ------------------------------------------------------------------ host ----
@@ -603,7 +990,28 @@ Variant pick(int n_max) {
     return variant<Cfg<D, 4, 8, 1>>();
 }
 
-Variant pick_variant(int d, int n_max) { return d == 64 ? pick<64>(n_max) : pick<128>(n_max); }
+cudaError_t launch_tc(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
+    k_attn_tc<<<grid, TcCfg::THREADS, TcCfg::SMEM, s>>>(mk, mv, a);
+    return cudaGetLastError();
+}
+
+// Kernel choice: the tcgen05 kernel for head_dim 128 and trees of at most 128
+// nodes unless TREESPEC_ATTN_KERNEL=mma asks for the mma.sync kernel.
+// Measured on GB300: for trees of up to 32 nodes the mma.sync kernel wins
+// (only one softmax warp of the tcgen05 kernel has rows to work on); from 33
+// nodes on, the tcgen05 kernel's tensor-core throughput wins.
+bool use_tc(int d, int n_max) {
+    if (d != 128 || n_max > TcCfg::NODES) return false;
+    const char *e = getenv("TREESPEC_ATTN_KERNEL");
+    if (e && strcmp(e, "mma") == 0) return false;
+    if (e && strcmp(e, "tc") == 0) return true;
+    return n_max > 32;
+}
+
+Variant pick_variant(int d, int n_max) {
+    if (use_tc(d, n_max)) return Variant{TcCfg::NODES, TcCfg::THREADS, TcCfg::SMEM, (const void *)k_attn_tc, launch_tc};
+    return d == 64 ? pick<64>(n_max) : pick<128>(n_max);
+}
 
 int occupancy(const Variant &v) {
     int occ = 0;
@@ -633,9 +1041,13 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
     const int tiles = (L_max + TK - 1) / TK;
     const long long pairs = (long long)B * H;
     const long long slots = (long long)num_sms() * occupancy(v);
+    // Split the key axis only when the (request, head) pairs fill at most half
+    // a wave of CTA slots: every split costs a prologue and a partial write, and
+    // splitting 256 pairs over 304 slots measured 1.7x slower than not.
     int splits = 1;
-    if (pairs < slots) splits = (int)((slots + pairs - 1) / pairs);
-    if (const char *e = getenv("TREESPEC_ATTN_SPLITS")) splits = atoi(e);
+    if (2 * pairs <= slots) splits = (int)((slots + pairs - 1) / pairs);
+    if (const char *e = getenv("TREESPEC_ATTN_SPLITS"))
+        if (*e) splits = atoi(e);
     splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
     splits = splits > tiles ? tiles : splits;
     p.chunk_tiles = (tiles + splits - 1) / splits;

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
 // ------------------------------------------------------------------- MSS ----
 constexpr int kMssThreads = 1024;
 constexpr int kMssWarps = kMssThreads / 32;
+constexpr float kL2E = 1.4426950408889634f;
 
 // float-float accumulation (Knuth two-sum)
 __device__ __forceinline__ void ff_add(float &hi, float &lo, float bh, float bl) {
@@ -214,15 +215,31 @@ struct MssShared {
     int bcast_i;
     int pick;
 };
+constexpr size_t kMssHeader = (sizeof(MssShared) + 15) & ~(size_t)15;
 
-// Residual value at y: R_0 = e(y) / Z, R_{j+1} = max(0, R_j - S_j q_j(y)).
-// The scalar acceptance test and every vector pass use this same function.
-__device__ __forceinline__ float resid_at(const float *row, const float *const *rq, const float *rS, int nrej,
-                                          int y, float invT, float m, float invZ) {
-    float r = expf(__fmaf_rn(__ldg(row + y), invT, -m)) * invZ;
-    for (int j = 0; j < nrej; ++j) r = fmaxf(0.f, __fmaf_rn(-rS[j], __ldg(rq[j] + y), r));
-    return r;
+// The residual of the current node. With the shared-memory row (R != nullptr)
+// R[y] holds it directly; otherwise it is recomputed from the logits and the
+// drafter rows of the rejections applied so far:
+//   R_0(y) = e(y) = 2^((l_y / T - m) log2 e),  R_{j+1}(y) = max(0, R_j(y) - S_j q_j(y))
+// with S_j = sum_y R_j(y); r_j = R_j / S_j is the normalised residual.
+struct Resid {
+    const float *row;
+    float invT, m;
+    const float *const *rq;
+    const float *rS;
+    int nrej;
+    const float *R;
+};
+
+__device__ __forceinline__ float e_of(float l, float invT, float m) { return exp2f((l * invT - m) * kL2E); }
+
+__device__ __forceinline__ float resid_recompute(const Resid &r, int y) {
+    float v = e_of(__ldg(r.row + y), r.invT, r.m);
+    for (int j = 0; j < r.nrej; ++j) v = fmaxf(0.f, __fmaf_rn(-r.rS[j], __ldg(r.rq[j] + y), v));
+    return v;
 }
+
+__device__ __forceinline__ float resid_at(const Resid &r, int y) { return r.R ? r.R[y] : resid_recompute(r, y); }
 
 __device__ double block_sum(MssShared &sm, float hi, float lo) {
 #pragma unroll
@@ -279,6 +296,11 @@ __device__ int block_or(MssShared &sm, int x) {
     return r;
 }
 
+// One CTA per request, walking the tree as Algorithm 2 does. SMEM_R keeps the
+// residual row of the current node in shared memory (vocabularies up to ~53K
+// entries): the exps are taken once per visited node and a rejection is one
+// in-place pass over R and one drafter row.
+template <bool SMEM_R>
 __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
                                                         const float *logits, const int32_t *p_row, int NP,
                                                         const float *ssm, const int32_t *q_row, int NQ,
@@ -286,6 +308,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                                                         uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     MssShared &sm = *reinterpret_cast<MssShared *>(smem_raw);
+    float *Rs = SMEM_R ? reinterpret_cast<float *>(smem_raw + kMssHeader) : nullptr;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int n = t.n_nodes[b];
     const int n_max = t.n_max;
@@ -329,7 +352,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
 
     for (int step = 0; step < n; ++step) {
         const float *row = logits + ((size_t)b * NP + sm.prow[u]) * V;
-        // pass 1: max of the tempered logits, finiteness
+        // pass 1: max of the tempered logits, finiteness (and the tempered row kept)
         float mx = -FLT_MAX;
         int nf = 0;
         if (vec) {
@@ -337,55 +360,56 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             for (int g = tid; g < V4; g += kMssThreads) {
                 float4 a = __ldg(r4 + g);
                 nf |= !isfinite(a.x) | !isfinite(a.y) | !isfinite(a.z) | !isfinite(a.w);
-                mx = fmaxf(mx, fmaxf(fmaxf(a.x * invT, a.y * invT), fmaxf(a.z * invT, a.w * invT)));
+                a.x *= invT; a.y *= invT; a.z *= invT; a.w *= invT;
+                mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+                if (SMEM_R) reinterpret_cast<float4 *>(Rs)[g] = a;
             }
         } else {
             for (int y = tid; y < V; y += kMssThreads) {
                 float a = __ldg(row + y);
                 nf |= !isfinite(a);
                 mx = fmaxf(mx, a * invT);
+                if (SMEM_R) Rs[y] = a * invT;
             }
         }
         if (block_or(sm, nf)) { nonfinite = 1; break; }
         const float m = block_max(sm, mx);
-        // pass 2: Z = sum exp(l/T - m)
-        float hi = 0.f, lo = 0.f;
-        {
-            float s = 0.f, c = 0.f;
+        // pass 2: e = 2^((l/T - m) log2 e) and Z = sum e
+        float s = 0.f, cc = 0.f;
+        if (SMEM_R) {
             if (vec) {
-                const float4 *r4 = reinterpret_cast<const float4 *>(row);
                 for (int g = tid; g < V4; g += kMssThreads) {
-                    float4 a = __ldg(r4 + g);
-                    kahan(s, c, expf(__fmaf_rn(a.x, invT, -m)));
-                    kahan(s, c, expf(__fmaf_rn(a.y, invT, -m)));
-                    kahan(s, c, expf(__fmaf_rn(a.z, invT, -m)));
-                    kahan(s, c, expf(__fmaf_rn(a.w, invT, -m)));
+                    float4 a = reinterpret_cast<float4 *>(Rs)[g];
+                    a.x = exp2f((a.x - m) * kL2E); a.y = exp2f((a.y - m) * kL2E);
+                    a.z = exp2f((a.z - m) * kL2E); a.w = exp2f((a.w - m) * kL2E);
+                    kahan(s, cc, a.x); kahan(s, cc, a.y); kahan(s, cc, a.z); kahan(s, cc, a.w);
+                    reinterpret_cast<float4 *>(Rs)[g] = a;
                 }
             } else {
-                for (int y = tid; y < V; y += kMssThreads) kahan(s, c, expf(__fmaf_rn(__ldg(row + y), invT, -m)));
+                for (int y = tid; y < V; y += kMssThreads) {
+                    const float e = exp2f((Rs[y] - m) * kL2E);
+                    Rs[y] = e;
+                    kahan(s, cc, e);
+                }
             }
-            hi = s;
-            lo = -c;
+        } else {
+            for (int y = tid; y < V; y += kMssThreads) kahan(s, cc, e_of(__ldg(row + y), invT, m));
         }
-        const double Z = block_sum(sm, hi, lo);
-        const float invZ = (float)(1.0 / Z);
+        double S = block_sum(sm, s, -cc);
 
         // children in input order: u+1, sub_end[u+1], ... below sub_end[u]
         int nrej = 0;
-        double S = 1.0;
         int accepted = -1;
         for (int c = u + 1; c < sm.sub_end[u]; c = sm.sub_end[c]) {
             const float *qc = ssm + ((size_t)b * NQ + sm.qrow[c]) * V;
             const int x = sm.tok[c];
+            const Resid rr{row, invT, m, sm.rej_q, sm.rej_S, nrej, Rs};
             if (tid == 0) {
                 const float qx = __ldg(qc + x);
                 int acc = 0, bad = !isfinite(qx);
                 if (!bad) {
                     double a = 1.0;
-                    if (qx > 0.f) {
-                        const float rx = resid_at(row, sm.rej_q, sm.rej_S, nrej, x, invT, m, invZ);
-                        a = fmin(1.0, (double)rx / (S * (double)qx));
-                    }
+                    if (qx > 0.f) a = fmin(1.0, (double)resid_at(rr, x) / (S * (double)qx));
                     acc = (double)u_acc[sm.perm[c]] <= a;
                 }
                 sm.pick = bad ? -2 : acc;
@@ -395,18 +419,27 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             __syncthreads();
             if (verdict == -2) { nonfinite = 1; break; }
             if (verdict == 1) { accepted = c; break; }
-            // rejection: S' = sum_y max(0, R(y) - S q_c(y))
+            // rejection: R' = max(0, R - S q_c), S' = sum R'
             const float Sf = (float)S;
-            float s = 0.f, cc = 0.f;
+            float s2 = 0.f, c2 = 0.f;
             int bad = 0;
-            for (int y = tid; y < V; y += kMssThreads) {
-                const float qy = __ldg(qc + y);
-                bad |= !isfinite(qy);
-                const float r = resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ);
-                kahan(s, cc, fmaxf(0.f, __fmaf_rn(-Sf, qy, r)));
+            if (SMEM_R) {
+                for (int y = tid; y < V; y += kMssThreads) {
+                    const float qy = __ldg(qc + y);
+                    bad |= !isfinite(qy);
+                    const float v = fmaxf(0.f, __fmaf_rn(-Sf, qy, Rs[y]));
+                    Rs[y] = v;
+                    kahan(s2, c2, v);
+                }
+            } else {
+                for (int y = tid; y < V; y += kMssThreads) {
+                    const float qy = __ldg(qc + y);
+                    bad |= !isfinite(qy);
+                    kahan(s2, c2, fmaxf(0.f, __fmaf_rn(-Sf, qy, resid_recompute(rr, y))));
+                }
             }
             if (block_or(sm, bad)) { nonfinite = 1; break; }
-            const double Snew = block_sum(sm, s, -cc);
+            const double Snew = block_sum(sm, s2, -c2);
             if (Snew > 0.0) {
                 if (tid == 0) {
                     sm.rej_q[nrej] = qc;
@@ -415,8 +448,13 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                 __syncthreads();
                 ++nrej;
                 S = Snew;
-            } else if (tid == 0) {
-                flag(status, TS_STATUS_ZERO_RESID);   // keep the residual unchanged
+            } else {
+                if (tid == 0) flag(status, TS_STATUS_ZERO_RESID);   // keep the residual unchanged
+                if (SMEM_R) {     // the in-place pass overwrote it: rebuild R from the applied rejections
+                    const Resid keep{row, invT, m, sm.rej_q, sm.rej_S, nrej, nullptr};
+                    for (int y = tid; y < V; y += kMssThreads) Rs[y] = resid_recompute(keep, y);
+                    __syncthreads();
+                }
             }
         }
         if (nonfinite) break;
@@ -427,16 +465,18 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             }
             ++cnt;
             u = accepted;
+            __syncthreads();   // the next node's pass 1 overwrites R
             continue;
         }
         // inverse CDF of the residual: contiguous segments per thread, fp64 scan
+        const Resid rr{row, invT, m, sm.rej_q, sm.rej_S, nrej, Rs};
         const int per = vec ? (V4 + kMssThreads - 1) / kMssThreads : (V + kMssThreads - 1) / kMssThreads;
         const int unit = vec ? 4 : 1;
         const int y0 = tid * per * unit, y1 = min(V, y0 + per * unit);
         {
-            float s = 0.f, cc = 0.f;
-            for (int y = y0; y < y1; ++y) kahan(s, cc, resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ));
-            sm.seg[tid] = (double)s - (double)cc;
+            float s3 = 0.f, c3 = 0.f;
+            for (int y = y0; y < y1; ++y) kahan(s3, c3, resid_at(rr, y));
+            sm.seg[tid] = (double)s3 - (double)c3;
         }
         __syncthreads();
         if (tid < 32) {     // exclusive scan of 1024 segment sums in fp64 by warp 0
@@ -467,6 +507,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         }
         __syncthreads();
         if (sm.pick == INT_MAX) {   // rounding left no bracket: the last segment with mass
+            __syncthreads();
             if (tid == 0) sm.pick = -1;
             __syncthreads();
             const double lo_c = sm.seg[tid];
@@ -479,7 +520,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             if (sm.pick >= 0) {
                 double cum = sm.seg[tid];
                 for (int y = y0; y < y1; ++y) {
-                    const float r = resid_at(row, sm.rej_q, sm.rej_S, nrej, y, invT, m, invZ);
+                    const float r = resid_at(rr, y);
                     cum += (double)r;
                     if (r > 0.f) last_pos = y;
                     if (r > 0.f && cum > target) { chosen = y; break; }
@@ -528,11 +569,19 @@ cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *o
                               const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
                               const float *uniforms, float temperature, const ts_tree &t, int V,
                               uint32_t *status, cudaStream_t s) {
-    const size_t smem = sizeof(MssShared);   // below the 48 KB default limit
-    const bool vec = (V % 4 == 0) && ((uintptr_t)logits % 16 == 0);
-    if (!vec && V % 4 == 0) return cudaErrorMisalignedAddress;
-    k_mss<<<t.B, kMssThreads, smem, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row, NQ,
-                                         uniforms, 1.0f / temperature, t, V, status);
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const size_t with_row = kMssHeader + (size_t)((V + 3) & ~3) * sizeof(float);
+    if (with_row <= (size_t)optin) {
+        cudaError_t e = cudaFuncSetAttribute(k_mss<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_row);
+        if (e != cudaSuccess) return e;
+        k_mss<true><<<t.B, kMssThreads, with_row, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row,
+                                                      NQ, uniforms, 1.0f / temperature, t, V, status);
+    } else {
+        k_mss<false><<<t.B, kMssThreads, kMssHeader, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm,
+                                                         q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+    }
     return cudaGetLastError();
 }
 
