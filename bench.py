@@ -193,6 +193,31 @@ def oracle_nodes_per_s(w, budget_s: float):
     return float(np.sum(n_nodes)) / t_step, t_step, oracle.num_threads(), sample
 
 
+def _events(n, external):
+    import torch
+    kw = {"enable_timing": True}
+    if external:
+        kw["external"] = True     # record nodes inside a captured graph
+    return [torch.cuda.Event(**kw) for _ in range(n)]
+
+
+def enqueue_steps(s, kind, K, ev, att, ver, stream):
+    """K verification steps on `stream`, with timing events around the whole
+    and around each step's attention and verify launches."""
+    ev[0].record(stream)
+    for i in range(K):
+        s.build()
+        s.append()
+        att[2 * i].record(stream)
+        s.attend()
+        att[2 * i + 1].record(stream)
+        ver[2 * i].record(stream)
+        s.verify(kind)
+        ver[2 * i + 1].record(stream)
+        s.commit(kind)
+    ev[1].record(stream)
+
+
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -255,47 +280,61 @@ def run_ours(args):
         if dist:
             dist.barrier()
 
-    # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream)
+    # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream).
+    # The K steps are captured once into a CUDA graph (each step is the same five
+    # library calls; the graph removes the host launch overhead between them);
+    # event-record nodes around the attention and verify launches time them.
     for _ in range(args.warmup):
         s.run(kind)
     torch.cuda.synchronize()
+    K = args.steps
+    graph, launch_mode = None, "eager launches"
+    if not args.eager:
+        try:
+            ev, att, ver = _events(2, True), _events(2 * K, True), _events(2 * K, True)
+            graph = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream(device)
+            cs.wait_stream(stream)
+            with torch.cuda.graph(graph, stream=cs, capture_error_mode="relaxed"):
+                enqueue_steps(s, kind, K, ev, att, ver, torch.cuda.current_stream(device))
+            stream.wait_stream(cs)
+            graph.replay()
+            torch.cuda.synchronize()
+            launch_mode = "CUDA graph of the K steps"
+        except Exception as exc:     # no graph support for event nodes: time eager launches
+            graph = None
+            launch_mode = f"eager launches ({type(exc).__name__} capturing a graph)"
+            torch.cuda.synchronize()
+    if graph is None:
+        ev, att, ver = _events(2, False), _events(2 * K, False), _events(2 * K, False)
+
+    def timed_pass():
+        if graph is not None:
+            graph.replay()
+        else:
+            enqueue_steps(s, kind, K, ev, att, ver, stream)
+
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
     t_load0 = time.time()
     while time.time() - t_load0 < 0.6:      # keep the GPU loaded while the sampler starts
-        for _ in range(20):
-            s.run(kind)
+        timed_pass()
         torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ver = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        s.build()
-        s.append()
-        att[i][0].record(stream)
-        s.attend()
-        att[i][1].record(stream)
-        ver[i][0].record(stream)
-        s.verify(kind)
-        ver[i][1].record(stream)
-        s.commit(kind)
-    ev[1].record(stream)
+    timed_pass()
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
     t_load1 = time.time()
     while time.time() - t_load1 < 0.4:
-        for _ in range(20):
-            s.run(kind)
+        timed_pass()
         torch.cuda.synchronize()
     if sampler:
         sampler.stop()
     ms = ev[0].elapsed_time(ev[1])
-    t_att = sum(a.elapsed_time(b) for a, b in att) / args.steps
-    t_ver = sum(a.elapsed_time(b) for a, b in ver) / args.steps
+    t_att = sum(att[2 * i].elapsed_time(att[2 * i + 1]) for i in range(K)) / K
+    t_ver = sum(ver[2 * i].elapsed_time(ver[2 * i + 1]) for i in range(K)) / K
     if dist:
         tt = torch.tensor([ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -329,6 +368,7 @@ def run_ours(args):
             "config": {"workload": DESCR[args.config], "name": args.config, "batch": w.B, "heads": w.H,
                        "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
                        "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "launch": launch_mode,
                        "l2": f"inputs larger than L2: {abytes / 2**20:.0f} MiB of K/V+Q per step vs 129 MiB"},
             "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
             "attention_ms": t_att, "verify_ms": t_ver,
@@ -389,6 +429,7 @@ def main():
     ap.add_argument("--config", default="llama7b", choices=sorted(DESCR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch every step from the host instead of a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

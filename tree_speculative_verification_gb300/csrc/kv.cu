@@ -9,10 +9,14 @@
 namespace ts {
 namespace {
 
-// cache[b][h][P + dfs_of[v]] = new[b][v][h], 16-byte vectors.
-__global__ void __launch_bounds__(128) k_kv_append(uint4 *k_cache, uint4 *v_cache, const uint4 *k_new,
-                                                   const uint4 *v_new, const int32_t *prefix_len, ts_tree t,
-                                                   int H, int row_vec, int L_max, uint32_t *status) {
+constexpr int kKvThreads = 256;
+
+// cache[b][h][P + dfs_of[v]] = new[b][v][h], 16-byte vectors; one CTA per
+// (head, request), the request's depth-first map staged in shared memory and
+// four independent copies in flight per thread.
+__global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 *v_cache, const uint4 *k_new,
+                                                          const uint4 *v_new, const int32_t *prefix_len, ts_tree t,
+                                                          int H, int row_vec, int L_max, uint32_t *status) {
     const int b = blockIdx.y, h = blockIdx.x;
     const int n = t.n_nodes[b], P = prefix_len[b];
     if (n <= 0) return;
@@ -20,50 +24,87 @@ __global__ void __launch_bounds__(128) k_kv_append(uint4 *k_cache, uint4 *v_cach
         if (h == 0 && threadIdx.x == 0) flag(status, TS_STATUS_INDEX);
         return;
     }
-    const int32_t *dfs_of = t.dfs_of + (size_t)b * t.n_max;
+    __shared__ int dfs_s[kMaxNodes];
+    for (int v = threadIdx.x; v < n; v += kKvThreads) dfs_s[v] = t.dfs_of[(size_t)b * t.n_max + v];
+    __syncthreads();
     const size_t cache_base = ((size_t)b * H + h) * L_max + P;
     const int total = n * row_vec;
-    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int v = idx / row_vec, c = idx - v * row_vec;
-        const size_t src = (((size_t)b * t.n_max + v) * H + h) * row_vec + c;
-        const size_t dst = (cache_base + dfs_of[v]) * row_vec + c;
-        k_cache[dst] = k_new[src];
-        v_cache[dst] = v_new[src];
+    for (int base = threadIdx.x; base < total; base += 4 * kKvThreads) {
+        uint4 kv[4], vv[4];
+        size_t dst[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = base + k * kKvThreads;
+            if (idx < total) {
+                const int v = idx / row_vec, c = idx - v * row_vec;
+                const size_t src = (((size_t)b * t.n_max + v) * H + h) * row_vec + c;
+                dst[k] = (cache_base + dfs_s[v]) * row_vec + c;
+                kv[k] = __ldcs(k_new + src);
+                vv[k] = __ldcs(v_new + src);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (base + k * kKvThreads < total) {
+                k_cache[dst[k]] = kv[k];
+                v_cache[dst[k]] = vv[k];
+            }
     }
 }
 
-// One warp per (b, h). Path node i moves from row P + dfs(path[i]) to row
-// P + i. Since dfs(path[i]) >= i (a node's DFS index is at least its depth),
-// handling the rows in increasing i never overwrites a row still to be read,
-// and every lane touches the same 16-byte column in every row.
-__global__ void __launch_bounds__(32) k_kv_commit(uint4 *k_cache, uint4 *v_cache, const int32_t *prefix_len,
-                                                  int32_t *new_prefix_len, const int32_t *out_path,
-                                                  const int32_t *out_count, ts_tree t, int H, int row_vec,
-                                                  int L_max, uint32_t *status) {
-    const int b = blockIdx.y, h = blockIdx.x, lane = threadIdx.x;
+// One CTA per (head, request). Path node i moves from row P + dfs(path[i]) to
+// row P + i. In each round every thread first reads its 16-byte pieces and,
+// after a barrier, writes them; a round's destinations (rows P + i) can never
+// be a later round's sources, because a node's DFS index is at least its
+// depth, dfs(path[i']) >= i'.
+__global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 *v_cache, const int32_t *prefix_len,
+                                                          int32_t *new_prefix_len, const int32_t *out_path,
+                                                          const int32_t *out_count, ts_tree t, int H, int row_vec,
+                                                          int L_max, uint32_t *status) {
+    const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
     const int n = t.n_nodes[b], P = prefix_len[b];
-    int cnt = out_count[b];
-    bool ok = n > 0 && cnt >= 0 && cnt <= n && P >= 0 && P + n <= L_max;
-    const int32_t *path = out_path + (size_t)b * (t.n_max + 1);
-    const int32_t *dfs_of = t.dfs_of + (size_t)b * t.n_max;
-    for (int i = 0; ok && i < cnt; ++i) ok = path[i] >= 0 && path[i] < n;
-    if (!ok) {
-        if (h == 0 && lane == 0) {
+    const int cnt = out_count[b];
+    __shared__ int src_s[kMaxNodes + 1];
+    __shared__ int bad_s;
+    if (tid == 0) bad_s = !(n > 0 && cnt >= 0 && cnt <= n && P >= 0 && P + n <= L_max);
+    __syncthreads();
+    if (!bad_s) {
+        const int32_t *path = out_path + (size_t)b * (t.n_max + 1);
+        for (int i = tid; i < cnt; i += kKvThreads) {
+            const int v = path[i];
+            if (v < 0 || v >= n) bad_s = 1;
+            else src_s[i] = t.dfs_of[(size_t)b * t.n_max + v];
+        }
+    }
+    __syncthreads();
+    if (bad_s) {
+        if (h == 0 && tid == 0) {
             if (cnt != 0 || (n > 0 && (P < 0 || P + n > L_max))) flag(status, TS_STATUS_INDEX);
             new_prefix_len[b] = P;
         }
         return;
     }
     const size_t base = ((size_t)b * H + h) * L_max + P;
-    for (int i = 0; i < cnt; ++i) {
-        const int src_row = dfs_of[path[i]];
-        if (src_row == i) continue;
-        for (int c = lane; c < row_vec; c += 32) {
-            k_cache[(base + i) * row_vec + c] = k_cache[(base + src_row) * row_vec + c];
-            v_cache[(base + i) * row_vec + c] = v_cache[(base + src_row) * row_vec + c];
+    const int total = cnt * row_vec;
+    for (int r0 = 0; r0 < total; r0 += kKvThreads) {
+        const int idx = r0 + tid;
+        uint4 kx, vx;
+        int i = 0, c = 0;
+        const bool mine = idx < total;
+        if (mine) {
+            i = idx / row_vec;
+            c = idx - i * row_vec;
+            kx = k_cache[(base + src_s[i]) * row_vec + c];
+            vx = v_cache[(base + src_s[i]) * row_vec + c];
         }
+        __syncthreads();
+        if (mine && src_s[i] != i) {
+            k_cache[(base + i) * row_vec + c] = kx;
+            v_cache[(base + i) * row_vec + c] = vx;
+        }
+        __syncthreads();
     }
-    if (h == 0 && lane == 0) new_prefix_len[b] = P + cnt;
+    if (h == 0 && tid == 0) new_prefix_len[b] = P + cnt;
 }
 
 }  // namespace
@@ -73,7 +114,7 @@ cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, co
                              uint32_t *status, cudaStream_t s) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
-    k_kv_append<<<grid, 128, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new,
+    k_kv_append<<<grid, kKvThreads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new,
                                      (const uint4 *)v_new, prefix_len, t, H, row_vec, L_max, status);
     return cudaGetLastError();
 }
@@ -83,7 +124,7 @@ cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix
                              int L_max, int esize, uint32_t *status, cudaStream_t s) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
-    k_kv_commit<<<grid, 32, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, prefix_len, new_prefix_len, out_path,
+    k_kv_commit<<<grid, kKvThreads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, prefix_len, new_prefix_len, out_path,
                                     out_count, t, H, row_vec, L_max, status);
     return cudaGetLastError();
 }

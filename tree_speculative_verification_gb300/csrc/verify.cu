@@ -57,34 +57,28 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
     int bi = INT_MAX;
     bool nf = false;
     if (vec4) {
+        // all of a thread's loads (up to 8 x 16 bytes) in flight at once
         const int V4 = V >> 2, per = (V4 + seg - 1) / seg;
         const int g0 = sg * per, g1 = min(V4, g0 + per);
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
-        int g = g0 + threadIdx.x;
-        for (; g + 3 * kGreedyThreads < g1; g += 4 * kGreedyThreads) {
-            float4 a[4];
+        for (int base = g0 + threadIdx.x; base < g1; base += 8 * kGreedyThreads) {
+            float4 a[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) a[k] = __ldcs(r4 + g + k * kGreedyThreads);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int i = 4 * (g + k * kGreedyThreads);
-                // the four loads cover increasing indices only within one float4, so
-                // compare with the tie rule across them
-                float xs[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (!isfinite(xs[e])) nf = true;
-                    if (better(xs[e], i + e, bv, bi)) { bv = xs[e]; bi = i + e; }
-                }
+            for (int k = 0; k < 8; ++k) {
+                const int g = base + k * kGreedyThreads;
+                if (g < g1) a[k] = __ldcs(r4 + g);
             }
-        }
-        for (; g < g1; g += kGreedyThreads) {
-            float4 a = __ldcs(r4 + g);
-            float xs[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (!isfinite(xs[e])) nf = true;
-                if (better(xs[e], 4 * g + e, bv, bi)) { bv = xs[e]; bi = 4 * g + e; }
+            for (int k = 0; k < 8; ++k) {
+                const int g = base + k * kGreedyThreads;
+                if (g < g1) {
+                    const float xs[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (!isfinite(xs[e])) nf = true;
+                        if (better(xs[e], 4 * g + e, bv, bi)) { bv = xs[e]; bi = 4 * g + e; }
+                    }
+                }
             }
         }
     } else {
@@ -129,15 +123,20 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
     // ---- last CTA of request b: merge segments, then walk (Algorithm 2, VerifyGreedy)
     __threadfence();
     __shared__ int am[kMaxNodes];
+    __shared__ int s_perm[kMaxNodes], s_tok[kMaxNodes], s_se[kMaxNodes];
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
     for (int w = threadIdx.x; w < n; w += kGreedyThreads) {
+        const size_t o = (size_t)b * n_max + w;
+        s_perm[w] = t.perm[o];
+        s_tok[w] = t.token[o];
+        s_se[w] = t.sub_end[o];
         float cv = -FLT_MAX;
         int ci = INT_MAX;
         bool bad = false;
         for (int k = 0; k < seg; ++k) {
-            const ArgPart *pp = parts + ((size_t)b * n_max + w) * seg + k;
+            const ArgPart *pp = parts + o * seg + k;
             float pv = __ldcg(&pp->val);
             int pi = __ldcg(&pp->idx);
             if (pi < 0) bad = true;
@@ -145,30 +144,27 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
         }
         am[w] = bad ? -1 : ci;
         if (bad) s_bad = 1;
-        if (argmax_out) argmax_out[(size_t)b * n_max + w] = am[w];
+        if (argmax_out) argmax_out[o] = am[w];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         counters[b] = 0u;   // leave the workspace zeroed for the next call
         int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
         int32_t *op = out_path + (size_t)b * (n_max + 1);
-        const int32_t *perm = t.perm + (size_t)b * n_max;
-        const int32_t *tok = t.token + (size_t)b * n_max;
-        const int32_t *se = t.sub_end + (size_t)b * n_max;
         if (s_bad) {
             out_count[b] = 0;
             flag(status, TS_STATUS_NONFINITE);
         } else {
             int u = 0, cnt = 0;
-            op[0] = perm[0];
+            op[0] = s_perm[0];
             for (int step = 0; step < n; ++step) {
-                const int o = am[perm[u]];
+                const int o = am[s_perm[u]];
                 int next = -1;
-                for (int c = u + 1; c < se[u]; c = se[c])
-                    if (tok[c] == o) { next = c; break; }
+                for (int c = u + 1; c < s_se[u]; c = s_se[c])
+                    if (s_tok[c] == o) { next = c; break; }
                 ot[cnt++] = o;
                 if (next < 0) break;
-                op[cnt] = perm[next];
+                op[cnt] = s_perm[next];
                 u = next;
             }
             out_count[b] = cnt;
