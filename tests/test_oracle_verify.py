@@ -399,3 +399,43 @@ def test_mss_nonfinite_only_where_read():
     r = oracle.verify_mss(logits, ssm, np.zeros((2, 3), np.int32), uni, par, tok, [3, 3])
     assert r["status"][0] & oracle.OR_NONFINITE and r["count"][0] == 0
     assert r["status"][1] == 0 and r["count"][1] == 3
+
+
+def test_naive_law_and_rejection_closed_form():
+    """Naive sampling (SpecInfer sec. 4.3): the first token is a draw from p, and
+    the walk stops at the root exactly when that draw is not a child token, so
+    the rejection rate is 1 - sum_{x in children} p(x)."""
+    rng = np.random.default_rng(21)
+    V, B = 8, 200_000
+    z = rng.standard_normal(V) * 1.5
+    p = np.exp(z - z.max()); p /= p.sum()
+    kids = np.array([1, 4, 4], np.int32)           # a duplicate child token counts once
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), (B, 1))
+    tok = np.tile(np.concatenate([[0], kids]).astype(np.int32), (B, 1))
+    logits = np.tile(z.astype(np.float32), (B, 4, 1))
+    uni = rng.random((B, 2, 4)).astype(np.float32)
+    r = oracle.verify_naive(logits, par, tok, np.full(B, 4), uni)
+    first = r["tokens"][:, 0]
+    assert stats.chisquare(np.bincount(first, minlength=V), p * B).pvalue > 1e-3
+    rej = np.mean(r["count"] == 1)
+    expect = 1.0 - p[1] - p[4]
+    assert abs(rej - expect) < 4 * np.sqrt(expect * (1 - expect) / B)
+
+
+def test_kv_commit_hand_built():
+    """Only the accepted path keeps its cache entries (SpecInfer sec. 4.2): path
+    node i moves to row P + i; every other row is untouched."""
+    B, H, L, d, n_max, P = 1, 2, 16, 4, 6, 5
+    cache = np.arange(B * H * L * d, dtype=np.float32).reshape(B, H, L, d)
+    dfs_of = np.array([[0, 3, 1, 5, 2, 4]], np.int32)      # input id -> DFS index
+    path = np.full((1, n_max + 1), -1, np.int32)
+    path[0, :3] = [0, 1, 3]                                  # root, then nodes at DFS 3 and 5
+    k2, v2, npl = oracle.kv_commit(cache, cache + 1000, [P], dfs_of, path, [3])
+    assert npl.tolist() == [P + 3]
+    for h in range(H):
+        assert np.array_equal(k2[0, h, P + 0], cache[0, h, P + 0])
+        assert np.array_equal(k2[0, h, P + 1], cache[0, h, P + 3])
+        assert np.array_equal(k2[0, h, P + 2], cache[0, h, P + 5])
+        assert np.array_equal(v2[0, h, P + 2], cache[0, h, P + 5] + 1000)
+        untouched = [r for r in range(L) if r not in (P, P + 1, P + 2)]
+        assert np.array_equal(k2[0, h, untouched], cache[0, h, untouched])
