@@ -265,7 +265,7 @@ def run_ours(args):
     from tree_speculative_verification_gb300 import api, workloads
     from tree_speculative_verification_gb300.step import DeviceStep
     api.load_library()
-    w = workloads.make(args.config)
+    w = workloads.make(args.config, scale_down=args.scale_down)
     s = DeviceStep(w, device)
     stream = torch.cuda.current_stream(device)
     kind = w.verify
@@ -365,7 +365,9 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": DESCR[args.config], "name": args.config, "batch": w.B, "heads": w.H,
+            "config": {"workload": DESCR[args.config] + (f" (batch and long prefix / {args.scale_down})"
+                                                         if args.scale_down > 1 else ""),
+                       "name": args.config, "batch": w.B, "heads": w.H,
                        "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
                        "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "launch": launch_mode,
@@ -430,6 +432,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host instead of a CUDA graph")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="divide the batch (and the long prefix) by N: a smaller case of the same kernels, for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -86,6 +86,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Bounded wait: false after kWaitCycles without completion.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase);
+// The same wait taken by a whole warp, with one verdict for every lane, so that
+// warp-collective instructions after it are never reached by only part of it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t phase) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase));
+}
+
+// Bounded wait: false after kWaitCycles without completion.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase) {
     if (mbar_try_wait(bar, phase)) return true;
     const long long t0 = clock64();
@@ -562,36 +570,43 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
 // ============================================================================
 // tcgen05 variant (trees of up to 128 nodes, head_dim 128).
 //
-// One CTA of 6 warps per (request, head, key chunk):
+// One CTA of 10 warps per (request, head, key chunk):
 //   warp 0    TMA producer (lane 0) and TMEM owner (alloc / dealloc)
 //   warp 1    MMA issuer (lane 0): S = Q K^T and O += P V with tcgen05.mma
-//   warps 2-5 softmax: thread r of TMEM lane quarter (warp % 4) owns node row
-//             r, reads its score row from TMEM, masks it, keeps a running max
-//             (rescaling O in TMEM only when the max grows by more than 2^8),
-//             writes bf16 P to shared memory.
-// Per 64-key tile: S (M = 128 node rows, N = 64 keys, K = 128) lands in one
-// of two TMEM score buffers; O (M = 128, N = 128, K = 64 keys) accumulates in
-// TMEM. Q, K and P are K-major, V is MN-major, all in the 128-byte swizzled
-// layout TMA writes. Every wait is bounded.
+//   warps 2-5 softmax stream 0 (even key tiles), warps 6-9 stream 1 (odd
+//             tiles): thread r of TMEM lane quarter (warp % 4) owns node row
+//             r, reads its score row from the stream's TMEM S buffer, masks
+//             it, keeps a running max (rescaling the stream's O in TMEM only
+//             when the max grows by more than 2^8), writes bf16 P to the
+//             stream's shared-memory P buffer.
+// The two streams have their own S (64 columns) and O (128 columns) in TMEM,
+// so the tensor core works on one stream while the other's softmax runs; at
+// the end the two (max, sum, O) partials are merged by log-sum-exp.
+// Per 64-key tile: S (M = 128 node rows, N = 64 keys, K = 128) and
+// O += P V (M = 128, N = 128, K = 64 keys). Q, K and P are K-major, V is
+// MN-major, all in the 128-byte swizzled layout TMA writes. Every wait is
+// bounded; TMEM is freed on every exit path.
 // ============================================================================
 struct TcCfg {
-    static constexpr int D = 128, TKT = 64, STAGES = 4, NODES = 128, THREADS = 192;
+    static constexpr int D = 128, TKT = 64, STAGES = 4, NODES = 128, STREAMS = 2;
+    static constexpr int THREADS = 64 + STREAMS * 128;
     static constexpr int BOX_BYTES = TKT * 128;           // 64 key rows x 128 bytes
     static constexpr int TILE_BYTES = 2 * BOX_BYTES;      // K (or V) of 64 keys x 128 dims
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
     static constexpr int QBOX = NODES * 128;              // 128 node rows x 64 dims
     static constexpr int Q_BYTES = 2 * QBOX;
-    static constexpr int P_BYTES = NODES * 128;           // 128 node rows x 64 keys
+    static constexpr int P_BYTES = NODES * 128;           // 128 node rows x 64 keys, one per stream
     static constexpr int ANC_WORDS = 4;                   // 128 nodes
     static constexpr int OFF_Q = STAGES * STAGE_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
-    static constexpr int OFF_ANC = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_ANC = OFF_P + STREAMS * P_BYTES;
     static constexpr int OFF_PERM = OFF_ANC + NODES * ANC_WORDS * 4;
-    static constexpr int NBAR = 2 * STAGES + 2 * 4 + 1;   // full, empty, s_full, s_free, p_full, pv_done, fin
-    static constexpr int OFF_BAR = OFF_PERM + NODES * 4;
+    static constexpr int OFF_ML = OFF_PERM + NODES * 4;   // stream 1's (max, sum) per row for the merge
+    static constexpr int NBAR = 2 * STAGES + 4 * STREAMS + 1;
+    static constexpr int OFF_BAR = OFF_ML + NODES * 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = 256;            // S0 [0,64), S1 [64,128), O [128,256)
+    static constexpr uint32_t TMEM_COLS = 512;            // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
 };
 
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -647,6 +662,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     const uint32_t sm_base = smem_u32(sm);
     uint32_t *anc_s = (uint32_t *)(sm + C::OFF_ANC);
     int *perm_s = (int *)(sm + C::OFF_PERM);
+    float2 *ml_s = (float2 *)(sm + C::OFF_ML);
     volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout, [2] merge flag
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -667,8 +683,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     const int row0 = (b * a.H + h) * a.L_max + k_begin;
 
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
-    const uint32_t s_full = empty + 8 * C::STAGES, s_free = s_full + 16, p_full = s_free + 16, pv_done = p_full + 16;
-    const uint32_t fin = pv_done + 16;
+    const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
+    const uint32_t pfull = sfree + 8 * C::STREAMS, pvdone = pfull + 8 * C::STREAMS;
+    const uint32_t fin = pvdone + 8 * C::STREAMS;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
@@ -681,11 +698,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full + 8 * x, 1);
-            mbar_init(s_free + 8 * x, 4);
-            mbar_init(p_full + 8 * x, 4);
-            mbar_init(pv_done + 8 * x, 1);
+        for (int x = 0; x < C::STREAMS; ++x) {
+            mbar_init(sfull + 8 * x, 1);
+            mbar_init(sfree + 8 * x, 4);
+            mbar_init(pfull + 8 * x, 4);
+            mbar_init(pvdone + 8 * x, 1);
         }
         mbar_init(fin, 1);
         misc[1] = 0;
@@ -695,11 +712,23 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
     for (int r = tid; r < C::NODES; r += C::THREADS) perm_s[r] = r < n ? t.perm[(size_t)b * n_max + r] : -1;
     __syncthreads();
-    for (int idx = tid; idx < C::NODES * 16; idx += C::THREADS) {
-        const int r = idx >> 4, c = idx & 15;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (r < n) val = ((const uint4 *)(a.q + (((size_t)b * n_max + perm_s[r]) * a.H + h) * D))[c];
-        *(uint4 *)(sm + C::OFF_Q + (c >> 3) * C::QBOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = val;
+    {
+        // every Q load of a thread issued before any of its stores
+        constexpr int PER = (C::NODES * 16 + C::THREADS - 1) / C::THREADS;
+        uint4 qv[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = tid + k * C::THREADS, r = idx >> 4, c = idx & 15;
+            qv[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < C::NODES * 16 && r < n)
+                qv[k] = __ldg((const uint4 *)(a.q + (((size_t)b * n_max + perm_s[r]) * a.H + h) * D) + c);
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = tid + k * C::THREADS, r = idx >> 4, c = idx & 15;
+            if (idx < C::NODES * 16)
+                *(uint4 *)(sm + C::OFF_Q + (c >> 3) * C::QBOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = qv[k];
+        }
     }
     for (int idx = tid; idx < C::NODES * C::ANC_WORDS; idx += C::THREADS) {
         const int r = idx / C::ANC_WORDS, w = idx % C::ANC_WORDS;
@@ -728,93 +757,97 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {   // ---------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
             const uint32_t q_base = sm_base + C::OFF_Q;
-            for (int j = 0; j <= ntiles && !misc[1]; ++j) {
-                if (j < ntiles) {
-                    const int st = j % C::STAGES;
-                    if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u) ||
-                        (j >= 2 && !mbar_wait_bounded(s_free + 8 * (j & 1), (uint32_t)((j >> 1) - 1) & 1u))) {
-                        misc[1] = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
+            // S of tile j into stream (j & 1)'s score buffer
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % C::STAGES, x = j & 1, k = j >> 1;
+                if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) return false;
+                if (k >= 1 && !mbar_wait_bounded(sfree + 8 * x, (uint32_t)(k - 1) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(q_base + (kk >> 2) * C::QBOX + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                        tc_mma(tmem + (j & 1) * C::TKT, ad, bd, idesc_s, kk > 0);
-                    }
-                    tc_commit(s_full + 8 * (j & 1));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(q_base + (kk >> 2) * C::QBOX + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
+                    tc_mma(tmem + x * C::TKT, ad, bd, idesc_s, kk > 0);
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, st2 = jj % C::STAGES;
-                    if (!mbar_wait_bounded(p_full + 8 * (jj & 1), (uint32_t)(jj >> 1) & 1u)) {
-                        misc[1] = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t pbase = sm_base + C::OFF_P + (jj & 1) * C::P_BYTES;
-                    const uint32_t vbase = sm_base + st2 * C::STAGE_BYTES + C::TILE_BYTES;
+                tc_commit(sfull + 8 * x);
+                return true;
+            };
+            bool ok = issue_s(0);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                if (j + 1 < ntiles && !(ok = issue_s(j + 1))) break;
+                const int x = j & 1, k = j >> 1, st = j % C::STAGES;
+                if (!mbar_wait_bounded(pfull + 8 * x, (uint32_t)k & 1u)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t pbase = sm_base + C::OFF_P + x * C::P_BYTES;
+                const uint32_t vbase = sm_base + st * C::STAGE_BYTES + C::TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < C::TKT / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
-                        tc_mma(tmem + 2 * C::TKT, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(empty + 8 * st2);
-                    tc_commit(pv_done + 8 * (jj & 1));
+                for (int kk = 0; kk < C::TKT / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
+                    tc_mma(tmem + 2 * C::TKT + x * D, ad, bd, idesc_pv, (k > 0 || kk > 0) ? 1u : 0u);
                 }
+                tc_commit(empty + 8 * st);
+                tc_commit(pvdone + 8 * x);
             }
+            if (!ok) misc[1] = 1;
             tc_commit(fin);   // completes once every MMA issued above has finished
             if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
         }
+        __syncwarp();
     } else {   // --------------------------------------------------------- softmax
-        const int wq = warp & 3, row = wq * 32 + lane;
+        const int x = (warp - 2) >> 2;                      // stream
+        const int wq = warp & 3, row = wq * 32 + lane;       // TMEM lane quarter, node row
         const bool active = wq * 32 < n;
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t s_col = x * C::TKT, o_col = 2 * C::TKT + x * D;
         uint32_t aw[C::ANC_WORDS];
 #pragma unroll
         for (int w = 0; w < C::ANC_WORDS; ++w) aw[w] = anc_s[row * C::ANC_WORDS + w];
         const float c = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntiles && ok; ++j) {
-            const int sb = j & 1;
-            if (!mbar_wait_bounded(s_full + 8 * sb, (uint32_t)(j >> 1) & 1u)) { ok = false; break; }
+        int k = 0;
+        for (int j = x; j < ntiles && ok; j += 2, ++k) {
+            if (!mbar_wait_warp(sfull + 8 * x, (uint32_t)k & 1u)) { ok = false; break; }
             tc_fence_after();
             float sv[64];
             if (active) {
-                tc_ld32(tl + sb * C::TKT, *reinterpret_cast<float(*)[32]>(&sv[0]));
-                tc_ld32(tl + sb * C::TKT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+                tc_ld32(tl + s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
+                tc_ld32(tl + s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
                 tc_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free + 8 * sb);
+            if (lane == 0) mbar_arrive(sfree + 8 * x);
+            const int key_base = k_begin + j * C::TKT;
+            // this stream's previous PV must be done before its O is rescaled or
+            // its P buffer rewritten
+            if (k >= 1 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(k - 1) & 1u)) { ok = false; break; }
             uint32_t pk[32];
             if (active) {
-                const int key_base = k_begin + j * C::TKT;
                 if (key_base + C::TKT > P || key_base + C::TKT > k_end) {
 #pragma unroll
-                    for (int k = 0; k < C::TKT; ++k) {
-                        const int key = key_base + k;
+                    for (int e = 0; e < C::TKT; ++e) {
+                        const int key = key_base + e;
                         bool vis = key < k_end;
                         if (vis && key >= P) {
                             const int tk = key - P;
                             vis = (aw[tk >> 5] >> (tk & 31)) & 1u;
                         }
-                        if (!vis) sv[k] = -INFINITY;
+                        if (!vis) sv[e] = -INFINITY;
                     }
                 }
-                float mt = sv[0];
+                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};   // four independent chains
 #pragma unroll
-                for (int k = 1; k < C::TKT; ++k) mt = fmaxf(mt, sv[k]);
-                mt *= c;
+                for (int e = 4; e < C::TKT; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+                const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
                 float alpha = 1.f;
                 bool resc = false;
                 if (m_run == -INFINITY) {
@@ -825,53 +858,44 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
                     resc = true;
                 }
                 if (__any_sync(0xffffffffu, resc)) {
-                    // O must hold every earlier tile before it is rescaled
-                    if (j >= 1 && !mbar_wait_bounded(pv_done + 8 * ((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u)) {
-                        ok = false;
-                    } else {
-                        tc_fence_after();
+                    tc_fence_after();
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float o[32];
-                            tc_ld32(tl + 2 * C::TKT + q4 * 32, o);
-                            tc_wait_ld();
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float o[32];
+                        tc_ld32(tl + o_col + q4 * 32, o);
+                        tc_wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                            tc_st32(tl + 2 * C::TKT + q4 * 32, o);
-                        }
-                        tc_wait_st();
-                        l_run *= alpha;
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tc_st32(tl + o_col + q4 * 32, o);
                     }
+                    tc_wait_st();
+                    l_run *= alpha;
                 }
                 const float mu = m_run == -INFINITY ? 0.f : m_run;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < C::TKT; k += 2) {
+                for (int e = 0; e < C::TKT; e += 2) {
                     float r0, r1;
-                    pk[k >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[k], c, -mu)), exp2f(__fmaf_rn(sv[k + 1], c, -mu)), r0, r1);
-                    l_run += r0 + r1;
+                    pk[e >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[e], c, -mu)), exp2f(__fmaf_rn(sv[e + 1], c, -mu)), r0, r1);
+                    ls[(e >> 1) & 3] += r0 + r1;
                 }
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             }
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            {
+            if (key_base + C::TKT > k_end) {
                 // last tile: V rows past the chunk may hold anything (even NaN);
                 // zero them before the PV reads the stage, so 0 * V stays 0
-                const int key_base = k_begin + j * C::TKT;
-                if (key_base + C::TKT > k_end) {
-                    const int st = j % C::STAGES;
-                    if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) { ok = false; break; }
-                    unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
-                    const int r0 = k_end - key_base;
-                    for (int idx = tid - 64; idx < (C::TKT - r0) * 16; idx += 128) {
-                        const int r = r0 + (idx >> 4), c16 = idx & 15;
-                        *(uint4 *)(vt + (c16 >> 3) * C::BOX_BYTES + r * 128 + ((c16 & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_async_smem();
+                const int st = j % C::STAGES;
+                if (!mbar_wait_warp(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) { ok = false; break; }
+                unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
+                const int r0 = k_end - key_base;
+                for (int idx = tid - 64 - 128 * x; idx < (C::TKT - r0) * 16; idx += 128) {
+                    const int r = r0 + (idx >> 4), c16 = idx & 15;
+                    *(uint4 *)(vt + (c16 >> 3) * C::BOX_BYTES + r * 128 + ((c16 & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_async_smem();
             }
-            // the P buffer of tile j was read by the PV of tile j - 2
-            if (j >= 2 && !mbar_wait_bounded(pv_done + 8 * sb, (uint32_t)((j >> 1) - 1) & 1u)) { ok = false; break; }
             if (active) {
-                unsigned char *prow = sm + C::OFF_P + sb * C::P_BYTES + row * 128;
+                unsigned char *prow = sm + C::OFF_P + x * C::P_BYTES + row * 128;
 #pragma unroll
                 for (int c16 = 0; c16 < 8; ++c16)
                     *(uint4 *)(prow + ((c16 ^ (row & 7)) << 4)) =
@@ -880,43 +904,62 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + 8 * sb);
+            if (lane == 0) mbar_arrive(pfull + 8 * x);
         }
+        // this stream's O is complete once its last PV has finished
+        const int nk = (ntiles - x + 1) / 2;                 // tiles this stream processed
+        if (ok && nk > 0 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(nk - 1) & 1u)) ok = false;
         if (!ok) misc[1] = 1;
-        // O is complete once the last PV has finished
-        if (ok && mbar_wait_bounded(pv_done + 8 * ((ntiles - 1) & 1), (uint32_t)((ntiles - 1) >> 1) & 1u)) {
-            tc_fence_after();
-            if (active) {
-                float o[D];
+        tc_fence_after();
+        if (x == 1) ml_s[row] = make_float2(nk > 0 ? m_run : -INFINITY, nk > 0 ? l_run : 0.f);
+        asm volatile("bar.sync 1, %0;" ::"n"(C::STREAMS * 128) : "memory");   // the softmax warps only
+        const int stop = __any_sync(0xffffffffu, misc[1]);   // one verdict per warp
+        if (x == 0 && active && !stop) {
+            // merge the two streams by log-sum-exp, then write the row
+            const float2 m1 = ml_s[row];
+            const float M = fmaxf(m_run, m1.x);
+            const float f0 = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
+            const float f1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
+            const float lsum = l_run * f0 + m1.y * f1;
+            float o[D];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tc_ld32(tl + 2 * C::TKT + q4 * 32, *reinterpret_cast<float(*)[32]>(&o[q4 * 32]));
-                tc_wait_ld();
-                if (row < n) {
-                    if (S_b == 1) {
-                        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                        uint4 *dst = (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D);
+            for (int q4 = 0; q4 < 4; ++q4) tc_ld32(tl + 2 * C::TKT + q4 * 32, *reinterpret_cast<float(*)[32]>(&o[q4 * 32]));
+            tc_wait_ld();
 #pragma unroll
-                        for (int c16 = 0; c16 < D / 8; ++c16) {
-                            float dummy0, dummy1;
-                            uint4 v;
-                            v.x = pack_bf16(o[8 * c16] * inv, o[8 * c16 + 1] * inv, dummy0, dummy1);
-                            v.y = pack_bf16(o[8 * c16 + 2] * inv, o[8 * c16 + 3] * inv, dummy0, dummy1);
-                            v.z = pack_bf16(o[8 * c16 + 4] * inv, o[8 * c16 + 5] * inv, dummy0, dummy1);
-                            v.w = pack_bf16(o[8 * c16 + 6] * inv, o[8 * c16 + 7] * inv, dummy0, dummy1);
-                            dst[c16] = v;
-                        }
-                    } else {
-                        const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
-                        a.part_ml[ps * 2 * a.n_pad + row] = m_run;
-                        a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = l_run;
-                        float4 *po = (float4 *)(a.part_o + (ps * a.n_pad + row) * D);
+            for (int e = 0; e < D; ++e) o[e] *= f0;
+            if (ntiles >= 2) {   // stream 1 wrote O1 (rows it never saw hold zeros there); CTA-uniform
 #pragma unroll
-                        for (int c4 = 0; c4 < D / 4; ++c4) po[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
-                    }
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float o1[32];
+                    tc_ld32(tl + 2 * C::TKT + D + q4 * 32, o1);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[q4 * 32 + e] = __fmaf_rn(o1[e], f1, o[q4 * 32 + e]);
                 }
             }
-        } else {
-            misc[1] = 1;
+            if (row < n) {
+                if (S_b == 1) {
+                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    uint4 *dst = (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D);
+#pragma unroll
+                    for (int c16 = 0; c16 < D / 8; ++c16) {
+                        float dummy0, dummy1;
+                        uint4 v;
+                        v.x = pack_bf16(o[8 * c16] * inv, o[8 * c16 + 1] * inv, dummy0, dummy1);
+                        v.y = pack_bf16(o[8 * c16 + 2] * inv, o[8 * c16 + 3] * inv, dummy0, dummy1);
+                        v.z = pack_bf16(o[8 * c16 + 4] * inv, o[8 * c16 + 5] * inv, dummy0, dummy1);
+                        v.w = pack_bf16(o[8 * c16 + 6] * inv, o[8 * c16 + 7] * inv, dummy0, dummy1);
+                        dst[c16] = v;
+                    }
+                } else {
+                    const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
+                    a.part_ml[ps * 2 * a.n_pad + row] = M;
+                    a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = lsum;
+                    float4 *po = (float4 *)(a.part_o + (ps * a.n_pad + row) * D);
+#pragma unroll
+                    for (int c4 = 0; c4 < D / 4; ++c4) po[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+                }
+            }
         }
     }
     tc_fence_before();

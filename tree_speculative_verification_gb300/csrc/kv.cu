@@ -66,15 +66,14 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 
     const int cnt = out_count[b];
     __shared__ int src_s[kMaxNodes + 1];
     __shared__ int bad_s;
+    // the path entries are read alongside the counts (no dependent round trip)
+    const int32_t *path = out_path + (size_t)b * (t.n_max + 1);
+    const int v_mine = tid <= t.n_max ? path[tid] : -1;
     if (tid == 0) bad_s = !(n > 0 && cnt >= 0 && cnt <= n && P >= 0 && P + n <= L_max);
     __syncthreads();
-    if (!bad_s) {
-        const int32_t *path = out_path + (size_t)b * (t.n_max + 1);
-        for (int i = tid; i < cnt; i += kKvThreads) {
-            const int v = path[i];
-            if (v < 0 || v >= n) bad_s = 1;
-            else src_s[i] = t.dfs_of[(size_t)b * t.n_max + v];
-        }
+    if (!bad_s && tid < cnt) {
+        if (v_mine < 0 || v_mine >= n) bad_s = 1;
+        else src_s[tid] = t.dfs_of[(size_t)b * t.n_max + v_mine];
     }
     __syncthreads();
     if (bad_s) {

@@ -21,7 +21,7 @@ namespace ts {
 namespace {
 
 // ---------------------------------------------------------------- greedy ----
-constexpr int kGreedyThreads = 256;
+constexpr int kGreedyThreads = 128;
 constexpr int kMaxSeg = 8;
 
 struct ArgPart {
@@ -135,13 +135,19 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
         float cv = -FLT_MAX;
         int ci = INT_MAX;
         bool bad = false;
-        for (int k = 0; k < seg; ++k) {
-            const ArgPart *pp = parts + o * seg + k;
-            float pv = __ldcg(&pp->val);
-            int pi = __ldcg(&pp->idx);
-            if (pi < 0) bad = true;
-            else if (better(pv, pi, cv, ci)) { cv = pv; ci = pi; }
-        }
+        ArgPart pp[kMaxSeg];   // all segment results of the node fetched at once
+#pragma unroll
+        for (int k = 0; k < kMaxSeg; ++k)
+            if (k < seg) {
+                pp[k].val = __ldcg(&parts[o * seg + k].val);
+                pp[k].idx = __ldcg(&parts[o * seg + k].idx);
+            }
+#pragma unroll
+        for (int k = 0; k < kMaxSeg; ++k)
+            if (k < seg) {
+                if (pp[k].idx < 0) bad = true;
+                else if (better(pp[k].val, pp[k].idx, cv, ci)) { cv = pp[k].val; ci = pp[k].idx; }
+            }
         am[w] = bad ? -1 : ci;
         if (bad) s_bad = 1;
         if (argmax_out) argmax_out[o] = am[w];
@@ -198,7 +204,10 @@ struct MssShared {
     double red_d[kMssWarps];
     float red_f[kMssWarps];
     int red_i[kMssWarps];
-    double seg[kMssThreads];
+    float wh[kMssWarps], wl[kMssWarps];     // float-float warp totals of the CDF scan
+    float cq[kMaxNodes];                    // q_c(x_c) of each child of the current node
+    float cu[kMaxNodes];                    // its accept uniform
+    int depth[kMaxNodes];
     int perm[kMaxNodes];
     int tok[kMaxNodes];
     int sub_end[kMaxNodes];
@@ -207,9 +216,12 @@ struct MssShared {
     const float *rej_q[kMaxNodes];
     float rej_S[kMaxNodes];
     double bcast_d;
+    double base;
     float bcast_f;
+    float us;                               // the final-sample uniform of the current node
     int bcast_i;
     int pick;
+    int token;
 };
 constexpr size_t kMssHeader = (sizeof(MssShared) + 15) & ~(size_t)15;
 
@@ -322,6 +334,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         sm.perm[i] = v;
         sm.tok[i] = t.token[o];
         sm.sub_end[i] = t.sub_end[o];
+        sm.depth[i] = t.depth[o];
         const int pr = p_row ? p_row[(size_t)b * n_max + v] : v;
         sm.prow[i] = pr;
         if (pr < 0 || pr >= NP) bad_index = 1;
@@ -348,24 +361,55 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
 
     for (int step = 0; step < n; ++step) {
         const float *row = logits + ((size_t)b * NP + sm.prow[u]) * V;
+        // the values the walk tests at this node, fetched in parallel now rather
+        // than one at a time later: q_c(x_c) and the accept uniform of every
+        // child, the final-sample uniform of u
+        {
+            const int du = sm.depth[u], se_u = sm.sub_end[u];
+            for (int i = u + 1 + tid; i < se_u; i += kMssThreads)
+                if (sm.depth[i] == du + 1) {
+                    sm.cq[i] = __ldg(ssm + ((size_t)b * NQ + sm.qrow[i]) * V + sm.tok[i]);
+                    sm.cu[i] = __ldg(u_acc + sm.perm[i]);
+                }
+            if (tid == kMssThreads - 1) sm.us = __ldg(u_smp + sm.perm[u]);
+        }
         // pass 1: max of the tempered logits, finiteness (and the tempered row kept)
         float mx = -FLT_MAX;
         int nf = 0;
         if (vec) {
+            // four independent 16-byte loads in flight per thread
             const float4 *r4 = reinterpret_cast<const float4 *>(row);
-            for (int g = tid; g < V4; g += kMssThreads) {
-                float4 a = __ldg(r4 + g);
-                nf |= !isfinite(a.x) | !isfinite(a.y) | !isfinite(a.z) | !isfinite(a.w);
-                a.x *= invT; a.y *= invT; a.z *= invT; a.w *= invT;
-                mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
-                if (SMEM_R) reinterpret_cast<float4 *>(Rs)[g] = a;
+            for (int g0 = tid; g0 < V4; g0 += 4 * kMssThreads) {
+                float4 a[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (g0 + k * kMssThreads < V4) a[k] = __ldg(r4 + g0 + k * kMssThreads);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int g = g0 + k * kMssThreads;
+                    if (g < V4) {
+                        nf |= !isfinite(a[k].x) | !isfinite(a[k].y) | !isfinite(a[k].z) | !isfinite(a[k].w);
+                        a[k].x *= invT; a[k].y *= invT; a[k].z *= invT; a[k].w *= invT;
+                        mx = fmaxf(mx, fmaxf(fmaxf(a[k].x, a[k].y), fmaxf(a[k].z, a[k].w)));
+                        if (SMEM_R) reinterpret_cast<float4 *>(Rs)[g] = a[k];
+                    }
+                }
             }
         } else {
-            for (int y = tid; y < V; y += kMssThreads) {
-                float a = __ldg(row + y);
-                nf |= !isfinite(a);
-                mx = fmaxf(mx, a * invT);
-                if (SMEM_R) Rs[y] = a * invT;
+            for (int y0 = tid; y0 < V; y0 += 4 * kMssThreads) {
+                float a[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (y0 + k * kMssThreads < V) a[k] = __ldg(row + y0 + k * kMssThreads);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int y = y0 + k * kMssThreads;
+                    if (y < V) {
+                        nf |= !isfinite(a[k]);
+                        mx = fmaxf(mx, a[k] * invT);
+                        if (SMEM_R) Rs[y] = a[k] * invT;
+                    }
+                }
             }
         }
         if (block_or(sm, nf)) { nonfinite = 1; break; }
@@ -401,12 +445,12 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             const int x = sm.tok[c];
             const Resid rr{row, invT, m, sm.rej_q, sm.rej_S, nrej, Rs};
             if (tid == 0) {
-                const float qx = __ldg(qc + x);
+                const float qx = sm.cq[c];
                 int acc = 0, bad = !isfinite(qx);
                 if (!bad) {
                     double a = 1.0;
                     if (qx > 0.f) a = fmin(1.0, (double)resid_at(rr, x) / (S * (double)qx));
-                    acc = (double)u_acc[sm.perm[c]] <= a;
+                    acc = (double)sm.cu[c] <= a;
                 }
                 sm.pick = bad ? -2 : acc;
             }
@@ -419,13 +463,45 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             const float Sf = (float)S;
             float s2 = 0.f, c2 = 0.f;
             int bad = 0;
-            if (SMEM_R) {
-                for (int y = tid; y < V; y += kMssThreads) {
-                    const float qy = __ldg(qc + y);
-                    bad |= !isfinite(qy);
-                    const float v = fmaxf(0.f, __fmaf_rn(-Sf, qy, Rs[y]));
-                    Rs[y] = v;
-                    kahan(s2, c2, v);
+            if (SMEM_R && vec && ((uintptr_t)qc & 15u) == 0) {
+                const float4 *q4 = reinterpret_cast<const float4 *>(qc);
+                float4 *R4 = reinterpret_cast<float4 *>(Rs);
+                for (int g0 = tid; g0 < V4; g0 += 4 * kMssThreads) {
+                    float4 qv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (g0 + k * kMssThreads < V4) qv[k] = __ldg(q4 + g0 + k * kMssThreads);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int g = g0 + k * kMssThreads;
+                        if (g < V4) {
+                            bad |= !isfinite(qv[k].x) | !isfinite(qv[k].y) | !isfinite(qv[k].z) | !isfinite(qv[k].w);
+                            float4 r = R4[g];
+                            r.x = fmaxf(0.f, __fmaf_rn(-Sf, qv[k].x, r.x));
+                            r.y = fmaxf(0.f, __fmaf_rn(-Sf, qv[k].y, r.y));
+                            r.z = fmaxf(0.f, __fmaf_rn(-Sf, qv[k].z, r.z));
+                            r.w = fmaxf(0.f, __fmaf_rn(-Sf, qv[k].w, r.w));
+                            R4[g] = r;
+                            kahan(s2, c2, r.x); kahan(s2, c2, r.y); kahan(s2, c2, r.z); kahan(s2, c2, r.w);
+                        }
+                    }
+                }
+            } else if (SMEM_R) {
+                for (int y0 = tid; y0 < V; y0 += 4 * kMssThreads) {
+                    float qv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (y0 + k * kMssThreads < V) qv[k] = __ldg(qc + y0 + k * kMssThreads);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int y = y0 + k * kMssThreads;
+                        if (y < V) {
+                            bad |= !isfinite(qv[k]);
+                            const float v = fmaxf(0.f, __fmaf_rn(-Sf, qv[k], Rs[y]));
+                            Rs[y] = v;
+                            kahan(s2, c2, v);
+                        }
+                    }
                 }
             } else {
                 for (int y = tid; y < V; y += kMssThreads) {
@@ -464,66 +540,91 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             __syncthreads();   // the next node's pass 1 overwrites R
             continue;
         }
-        // inverse CDF of the residual: contiguous segments per thread, fp64 scan
+        // inverse CDF of the residual: the first y with C(y) > u * S. Each thread
+        // sums a contiguous segment (compensated fp32), a float-float block scan
+        // gives every segment's starting point, the segment holding u * S is
+        // found by a bracket test, and warp 0 scans inside it.
         const Resid rr{row, invT, m, sm.rej_q, sm.rej_S, nrej, Rs};
         const int per = vec ? (V4 + kMssThreads - 1) / kMssThreads : (V + kMssThreads - 1) / kMssThreads;
         const int unit = vec ? 4 : 1;
-        const int y0 = tid * per * unit, y1 = min(V, y0 + per * unit);
+        const int warp = tid >> 5, lane = tid & 31;
+        float sh, sl;
         {
+            const int y0 = tid * per * unit, y1 = min(V, y0 + per * unit);
             float s3 = 0.f, c3 = 0.f;
             for (int y = y0; y < y1; ++y) kahan(s3, c3, resid_at(rr, y));
-            sm.seg[tid] = (double)s3 - (double)c3;
+            sh = s3;
+            sl = -c3;
         }
-        __syncthreads();
-        if (tid < 32) {     // exclusive scan of 1024 segment sums in fp64 by warp 0
-            double run = 0.0;
-            for (int k = 0; k < 32; ++k) run += sm.seg[tid * 32 + k];
-            double incl = run;
+        float ih = sh, il = sl;     // inclusive warp scan (float-float)
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                double up = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += up;
-            }
-            double base = incl - run;
-            for (int k = 0; k < 32; ++k) {
-                double val = sm.seg[tid * 32 + k];
-                sm.seg[tid * 32 + k] = base;   // now the exclusive prefix
-                base += val;
-                if (k == 31 && tid == 31) sm.bcast_d = base;   // total
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+            const float bh = __shfl_up_sync(0xffffffffu, ih, o), bl = __shfl_up_sync(0xffffffffu, il, o);
+            if (lane >= o) ff_add(ih, il, bh, bl);
+        }
+        if (lane == 31) {
+            sm.wh[warp] = ih;
+            sm.wl[warp] = il;
         }
         if (tid == 0) sm.pick = INT_MAX;
         __syncthreads();
-        const double total = sm.bcast_d;
-        const double target = (double)u_smp[sm.perm[u]] * total;
-        {
-            const double lo_c = sm.seg[tid];
-            const double hi_c = tid + 1 < kMssThreads ? sm.seg[tid + 1] : total;
-            if (hi_c > lo_c && lo_c <= target && target < hi_c) atomicMin(&sm.pick, tid);
+        if (warp == 0) {            // exclusive scan of the 32 warp totals
+            const float oh = sm.wh[lane], ol = sm.wl[lane];
+            float xh = oh, xl = ol;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float bh = __shfl_up_sync(0xffffffffu, xh, o), bl = __shfl_up_sync(0xffffffffu, xl, o);
+                if (lane >= o) ff_add(xh, xl, bh, bl);
+            }
+            if (lane == 31) sm.bcast_d = (double)xh + (double)xl;   // total mass
+            ff_add(xh, xl, -oh, -ol);
+            __syncwarp();
+            sm.wh[lane] = xh;
+            sm.wl[lane] = xl;
         }
+        __syncthreads();
+        float ph = ih, pl = il;
+        ff_add(ph, pl, -sh, -sl);
+        ff_add(ph, pl, sm.wh[warp], sm.wl[warp]);
+        const double total = sm.bcast_d;
+        const double target = (double)sm.us * total;
+        const double lo_c = (double)ph + (double)pl, hi_c = lo_c + ((double)sh + (double)sl);
+        if (hi_c > lo_c && lo_c <= target && target < hi_c) atomicMin(&sm.pick, tid);
         __syncthreads();
         if (sm.pick == INT_MAX) {   // rounding left no bracket: the last segment with mass
             __syncthreads();
             if (tid == 0) sm.pick = -1;
             __syncthreads();
-            const double lo_c = sm.seg[tid];
-            const double hi_c = tid + 1 < kMssThreads ? sm.seg[tid + 1] : total;
             if (hi_c > lo_c) atomicMax(&sm.pick, tid);
             __syncthreads();
         }
-        if (tid == sm.pick || (sm.pick < 0 && tid == 0)) {
+        const int pick = sm.pick;
+        if (tid == pick) sm.base = lo_c;
+        __syncthreads();
+        if (warp == 0) {
             int chosen = -1, last_pos = -1;
-            if (sm.pick >= 0) {
-                double cum = sm.seg[tid];
-                for (int y = y0; y < y1; ++y) {
-                    const float r = resid_at(rr, y);
-                    cum += (double)r;
-                    if (r > 0.f) last_pos = y;
-                    if (r > 0.f && cum > target) { chosen = y; break; }
+            if (pick >= 0) {
+                const int ys = pick * per * unit, ye = min(V, ys + per * unit);
+                double carry = sm.base;
+                for (int y0 = ys; y0 < ye && chosen < 0; y0 += 32) {
+                    const int y = y0 + lane;
+                    const float r = y < ye ? resid_at(rr, y) : 0.f;
+                    float ch = r, cl = 0.f;   // inclusive scan of this 32-wide slice
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float bh = __shfl_up_sync(0xffffffffu, ch, o), bl = __shfl_up_sync(0xffffffffu, cl, o);
+                        if (lane >= o) ff_add(ch, cl, bh, bl);
+                    }
+                    const double cum = carry + ((double)ch + (double)cl);
+                    const unsigned hit = __ballot_sync(0xffffffffu, r > 0.f && cum > target);
+                    const unsigned pos = __ballot_sync(0xffffffffu, r > 0.f);
+                    if (hit) chosen = y0 + __ffs(hit) - 1;
+                    else if (pos) last_pos = y0 + 31 - __clz(pos);
+                    carry += (double)__shfl_sync(0xffffffffu, ch, 31) + (double)__shfl_sync(0xffffffffu, cl, 31);
                 }
             }
             if (chosen < 0) chosen = last_pos >= 0 ? last_pos : 0;
-            ot[cnt] = chosen;
+            if (lane == 0) ot[cnt] = chosen;
         }
         ++cnt;
         break;
@@ -549,9 +650,18 @@ size_t greedy_ws_bytes(int B, int n_max, int V) {
 cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *argmax_out,
                                  const float *logits, const ts_tree &t, int V, void *ws, uint32_t *status,
                                  cudaStream_t s) {
+    // vocab segments per node row: as many as fit one wave of resident CTAs
+    // (a second, partial wave doubles the time of this latency-bound pass),
+    // and no segment shorter than 2048 entries
+    static int occ = 0;
+    if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_greedy, kGreedyThreads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        occ = 4;
+    }
     const int rows = t.B * t.n_max;
-    int seg = (4 * num_sms() + rows - 1) / rows;
-    seg = max(1, min(kMaxSeg, min(seg, V / 2048 > 0 ? V / 2048 : 1)));
+    const int slots = num_sms() * (occ > 0 ? occ : 1);
+    int seg = slots / rows;
+    seg = max(1, min(kMaxSeg, min(seg, max(1, V / 2048))));
     const bool vec4 = (V % 4 == 0) && ((uintptr_t)logits % 16 == 0);
     unsigned *counters = (unsigned *)ws;
     ArgPart *parts = (ArgPart *)((char *)ws + ((size_t)t.B * sizeof(unsigned) + 255) / 256 * 256);
