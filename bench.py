@@ -60,9 +60,10 @@ def attention_bytes(w) -> int:
     return kv + qo
 
 
-def _traffic_from_profile(w):
+def _traffic_from_profile(w, kernel):
     """dram bytes per attention launch from the committed ncu summary, only if the
-    kernel source is unchanged since the capture (hash of attn_bf16.cu)."""
+    summary is of the kernel this run launches and the kernel source is
+    unchanged since the capture (hash of attn_bf16.cu)."""
     src = os.path.join(ROOT, "tree_speculative_verification_gb300", "csrc", "attn_bf16.cu")
     prof = os.path.join(ROOT, "profiles", f"tree_attention_{w.name}.md")
     try:
@@ -75,7 +76,7 @@ def _traffic_from_profile(w):
         if line.startswith("- ") and ":" in line:
             k, _, v = line[2:].partition(":")
             kv[k.strip()] = v.strip()
-    if kv.get("source_sha256_16") != h:
+    if kv.get("source_sha256_16") != h or kv.get("kernel") != kernel:
         return None
     try:
         return float(kv["dram_bytes_per_full_launch"])
@@ -201,19 +202,22 @@ def _events(n, external):
     return [torch.cuda.Event(**kw) for _ in range(n)]
 
 
-def enqueue_steps(s, kind, K, ev, att, ver, stream):
-    """K verification steps on `stream`, with timing events around the whole
-    and around each step's attention and verify launches."""
+def enqueue_steps(s, kind, K, ev, stream, att=None, ver=None):
+    """K verification steps on `stream` between the events ev[0], ev[1]; with
+    `att`/`ver`, also events around each step's attention and verify launches."""
     ev[0].record(stream)
     for i in range(K):
         s.build()
         s.append()
-        att[2 * i].record(stream)
+        if att is not None:
+            att[2 * i].record(stream)
         s.attend()
-        att[2 * i + 1].record(stream)
-        ver[2 * i].record(stream)
+        if att is not None:
+            att[2 * i + 1].record(stream)
+            ver[2 * i].record(stream)
         s.verify(kind)
-        ver[2 * i + 1].record(stream)
+        if ver is not None:
+            ver[2 * i + 1].record(stream)
         s.commit(kind)
     ev[1].record(stream)
 
@@ -282,37 +286,49 @@ def run_ours(args):
 
     # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream).
     # The K steps are captured once into a CUDA graph (each step is the same five
-    # library calls; the graph removes the host launch overhead between them);
-    # event-record nodes around the attention and verify launches time them.
+    # library calls; the graph removes the host launch overhead between them).
+    # The timed pass has events at its two ends only: an event-record node
+    # between two kernels of a graph costs a few microseconds. A second timed
+    # pass of the same K steps, captured with event nodes around every
+    # attention and verify launch, gives those kernels' durations.
     for _ in range(args.warmup):
         s.run(kind)
     torch.cuda.synchronize()
     K = args.steps
-    graph, launch_mode = None, "eager launches"
+    graphs, launch_mode = None, "eager launches"
+    ev, ev2, att, ver = (_events(2, not args.eager), _events(2, not args.eager), _events(2 * K, not args.eager),
+                         _events(2 * K, not args.eager))
     if not args.eager:
         try:
-            ev, att, ver = _events(2, True), _events(2 * K, True), _events(2 * K, True)
-            graph = torch.cuda.CUDAGraph()
-            cs = torch.cuda.Stream(device)
-            cs.wait_stream(stream)
-            with torch.cuda.graph(graph, stream=cs, capture_error_mode="relaxed"):
-                enqueue_steps(s, kind, K, ev, att, ver, torch.cuda.current_stream(device))
-            stream.wait_stream(cs)
-            graph.replay()
-            torch.cuda.synchronize()
+            graphs = []
+            for with_kernel_events in (False, True):
+                g = torch.cuda.CUDAGraph()
+                cs = torch.cuda.Stream(device)
+                cs.wait_stream(stream)
+                with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+                    cur = torch.cuda.current_stream(device)
+                    if with_kernel_events:
+                        enqueue_steps(s, kind, K, ev2, cur, att, ver)
+                    else:
+                        enqueue_steps(s, kind, K, ev, cur)
+                stream.wait_stream(cs)
+                g.replay()
+                torch.cuda.synchronize()
+                graphs.append(g)
             launch_mode = "CUDA graph of the K steps"
         except Exception as exc:     # no graph support for event nodes: time eager launches
-            graph = None
+            graphs = None
             launch_mode = f"eager launches ({type(exc).__name__} capturing a graph)"
             torch.cuda.synchronize()
-    if graph is None:
-        ev, att, ver = _events(2, False), _events(2 * K, False), _events(2 * K, False)
+            ev, ev2, att, ver = _events(2, False), _events(2, False), _events(2 * K, False), _events(2 * K, False)
 
-    def timed_pass():
-        if graph is not None:
-            graph.replay()
+    def timed_pass(with_kernel_events=False):
+        if graphs is not None:
+            graphs[1 if with_kernel_events else 0].replay()
+        elif with_kernel_events:
+            enqueue_steps(s, kind, K, ev2, stream, att, ver)
         else:
-            enqueue_steps(s, kind, K, ev, att, ver, stream)
+            enqueue_steps(s, kind, K, ev, stream)
 
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
     t_load0 = time.time()
@@ -326,6 +342,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
+    timed_pass(with_kernel_events=True)
+    torch.cuda.synchronize()
     t_load1 = time.time()
     while time.time() - t_load1 < 0.4:
         timed_pass()
@@ -333,6 +351,7 @@ def run_ours(args):
     if sampler:
         sampler.stop()
     ms = ev[0].elapsed_time(ev[1])
+    ms_kernel_events = ev2[0].elapsed_time(ev2[1])
     t_att = sum(att[2 * i].elapsed_time(att[2 * i + 1]) for i in range(K)) / K
     t_ver = sum(ver[2 * i].elapsed_time(ver[2 * i + 1]) for i in range(K)) / K
     if dist:
@@ -353,8 +372,9 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     abytes = attention_bytes(w)
     achieved = abytes / (t_att * 1e-3) / 1e9
+    kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": _traffic_from_profile(w), "kernel": "tree_attention (k_attn_bf16)",
+            "traffic": _traffic_from_profile(w, kernel), "kernel": f"tree_attention ({kernel})",
             "algorithmic_bytes_per_launch": abytes, "peak_kind": peak_kind,
             "avg_launch_us": t_att * 1e3}
     cpu = None
@@ -371,9 +391,11 @@ def run_ours(args):
                        "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
                        "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "launch": launch_mode,
+                       "kernel_timing": "attention and verify durations from a second timed pass of the same "
+                                        "K steps with event nodes around each of their launches",
                        "l2": f"inputs larger than L2: {abytes / 2**20:.0f} MiB of K/V+Q per step vs 129 MiB"},
             "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
-            "attention_ms": t_att, "verify_ms": t_ver,
+            "attention_ms": t_att, "verify_ms": t_ver, "ms_per_step_with_kernel_events": ms_kernel_events / args.steps,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * s.launches_per_step(kind)}
     print(json.dumps(line), flush=True)

@@ -251,6 +251,15 @@ ts_status tree_attention_noalloc(void *out, const void *q, const void *k_cache, 
 /* Bytes of workspace an op needs for these sizes on the current device (0 if none). */
 size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_max, int V);
 
+/*
+ * Name of the kernel tree_attention launches for these sizes on the current
+ * device ("k_attn_f32", "k_attn_bf16<D,NT,NG,KS>", "k_attn_tc" or
+ * "k_attn_tp"), as chosen by the same plan the launch uses (including the
+ * TREESPEC_ATTN_* environment overrides). Static string owned by the
+ * library; "" for sizes tree_attention would reject. No GPU work.
+ */
+const char *treespec_attention_kernel(int B, int H, int n_max, int d, int L_max, ts_dtype dtype);
+
 /* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
 ts_status treespec_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 

@@ -25,7 +25,7 @@ MAX_NODES = 256
 #: every entry point of the C ABI (include/treespec.h)
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
-           "treespec_version", "tree_attention_noalloc")
+           "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -72,6 +72,8 @@ def load_library(path: str | None = None):
         fn.restype = C.c_int
     lib.treespec_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.treespec_workspace_size.restype = C.c_size_t
+    lib.treespec_attention_kernel.argtypes = [I, I, I, I, I, I]
+    lib.treespec_attention_kernel.restype = C.c_char_p
     lib.treespec_last_error.restype = C.c_char_p
     lib.treespec_version.restype = C.c_char_p
     _lib = lib
@@ -166,6 +168,11 @@ def kv_append(k_cache, v_cache, k_new, v_new, prefix_len, tree: Tree, status=Non
 
 def workspace_size(op: int, B: int, H: int, n_max: int, d: int, L_max: int, V: int) -> int:
     return int(load_library().treespec_workspace_size(op, B, H, n_max, d, L_max, V))
+
+
+def attention_kernel(B: int, H: int, n_max: int, d: int, L_max: int, dtype: int) -> str:
+    """Name of the kernel tree_attention launches for these sizes ("" if rejected)."""
+    return load_library().treespec_attention_kernel(B, H, n_max, d, L_max, dtype).decode()
 
 
 def workspace(op: int, B: int, H: int = 1, n_max: int = 1, d: int = 128, L_max: int = 1, V: int = 1,

@@ -3,6 +3,7 @@
 // layouts and error behaviour, in include/treespec.h.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "ts_internal.cuh"
@@ -62,6 +63,16 @@ ts_status set_error(ts_status st, const char *fmt, ...) {
     vsnprintf(g_err, sizeof g_err, fmt, ap);
     va_end(ap);
     return st;
+}
+}  // namespace ts
+
+namespace ts {
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("TREESPEC_PDL");
+        return !(e && *e && atoi(e) == 0);
+    }();
+    return on;
 }
 }  // namespace ts
 
@@ -226,6 +237,13 @@ size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_m
         default:
             return 0;
     }
+}
+
+const char *treespec_attention_kernel(int B, int H, int n_max, int d, int L_max, ts_dtype dtype) {
+    if (B < 1 || H < 1 || n_max < 1 || n_max > TS_MAX_NODES || (d != 64 && d != 128) || L_max < n_max ||
+        (dtype != TS_F32 && dtype != TS_BF16))
+        return "";
+    return ts::attn_plan(B, H, n_max, d, L_max, dtype).kernel;
 }
 
 ts_status treespec_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {

@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "ts_internal.cuh"
@@ -217,6 +218,8 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
     const int g = lane >> 2, tq = lane & 3;
     const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
     const ts_tree &t = a.t;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b], P = a.prefix_len[b];
     if (n <= 0) return;
     if (P < 0 || P + n > a.L_max) {
@@ -668,6 +671,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
     const ts_tree &t = a.t;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b], P = a.prefix_len[b];
     if (n <= 0) return;
     if (P < 0 || P + n > a.L_max) {
@@ -1036,6 +1041,8 @@ __global__ void __launch_bounds__(TpCfg::THREADS, 1) k_attn_tp(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pairs = a.t.B * a.H, G = gridDim.x;
     const int n_max = a.t.n_max, W = TS_MASK_WORDS(n_max);
+    pdl_wait();
+    pdl_trigger();
 
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
     const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
@@ -1428,19 +1435,27 @@ bool make_map(CUtensorMap *map, const void *base, int d, long long rows) {
 
 struct Variant {
     int nodes, threads, smem;
+    const char *name;
     const void *fn;
     cudaError_t (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const AttnArgs &, cudaStream_t);
 };
 
 template <class C>
 cudaError_t launch_cfg(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
-    k_attn_bf16<C><<<grid, C::THREADS, C::SMEM, s>>>(mk, mv, a);
-    return cudaGetLastError();
+    return launch(k_attn_bf16<C>, grid, dim3(C::THREADS), C::SMEM, s, mk, mv, a);
+}
+
+template <class C>
+const char *cfg_name() {
+    static char buf[48];
+    static const bool once = (snprintf(buf, sizeof buf, "k_attn_bf16<%d,%d,%d,%d>", C::D, C::NT, C::NG, C::KS), true);
+    (void)once;
+    return buf;
 }
 
 template <class C>
 Variant variant() {
-    return Variant{C::NODES, C::THREADS, C::SMEM, (const void *)k_attn_bf16<C>, launch_cfg<C>};
+    return Variant{C::NODES, C::THREADS, C::SMEM, cfg_name<C>(), (const void *)k_attn_bf16<C>, launch_cfg<C>};
 }
 
 template <int D>
@@ -1456,8 +1471,7 @@ Variant pick(int n_max) {
 }
 
 cudaError_t launch_tc(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
-    k_attn_tc<<<grid, TcCfg::THREADS, TcCfg::SMEM, s>>>(mk, mv, a);
-    return cudaGetLastError();
+    return launch(k_attn_tc, grid, dim3(TcCfg::THREADS), TcCfg::SMEM, s, mk, mv, a);
 }
 
 // Kernel choice: the tcgen05 kernel for head_dim 128 and trees of at most 128
@@ -1474,7 +1488,8 @@ bool use_tc(int d, int n_max) {
 }
 
 Variant pick_variant(int d, int n_max) {
-    if (use_tc(d, n_max)) return Variant{TcCfg::NODES, TcCfg::THREADS, TcCfg::SMEM, (const void *)k_attn_tc, launch_tc};
+    if (use_tc(d, n_max))
+        return Variant{TcCfg::NODES, TcCfg::THREADS, TcCfg::SMEM, "k_attn_tc", (const void *)k_attn_tc, launch_tc};
     return d == 64 ? pick<64>(n_max) : pick<128>(n_max);
 }
 
@@ -1500,9 +1515,10 @@ int num_sms() {
 }
 
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
-    AttnPlan p{1, 1, 0, 0};
+    AttnPlan p{1, 1, 0, 0, false, "k_attn_f32"};
     if (dt != TS_BF16) return p;
     const Variant v = pick_variant(d, n_max);
+    p.kernel = v.name;
     const int tiles = (L_max + TK - 1) / TK;
     const long long pairs = (long long)B * H;
     const long long slots = (long long)num_sms() * occupancy(v);
@@ -1520,6 +1536,14 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
     p.n_pad = v.nodes;
     const size_t counters = ((size_t)pairs * 4 + 255) / 256 * 256;
     p.ws_bytes = p.splits > 1 ? counters + (size_t)pairs * p.splits * p.n_pad * (2 + d) * 4 : counters;
+    // The persistent tcgen05 kernel (CTAs walk the (request, head) items)
+    // measured faster only with many short items; TREESPEC_ATTN_PERSISTENT=0/1
+    // overrides.
+    const char *pe = getenv("TREESPEC_ATTN_PERSISTENT");
+    const bool many_items = pairs >= 8LL * num_sms();
+    const bool persistent = pe && *pe ? atoi(pe) != 0 : many_items;
+    p.persistent = p.splits == 1 && use_tc(d, n_max) && persistent;
+    if (p.persistent) p.kernel = "k_attn_tp";
     return p;
 }
 
@@ -1552,17 +1576,12 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
     a.part_ml = (float *)((char *)ws + counters);
     a.part_o = a.part_ml + pairs * plan.splits * 2 * plan.n_pad;
     a.status = status;
-    const char *pe = getenv("TREESPEC_ATTN_PERSISTENT");
-    const bool many_items = (long long)t.B * H >= 8LL * num_sms();   // measured: wins only with short, many items
-    const bool persistent = pe && *pe ? atoi(pe) != 0 : many_items;
-    if (plan.splits == 1 && use_tc(d, t.n_max) && persistent) {
-        // persistent tcgen05 kernel: CTAs walk the (request, head) items
+    if (plan.persistent) {
         e = cudaFuncSetAttribute(k_attn_tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpCfg::SMEM);
         if (e != cudaSuccess) return e;
         const int pairs = t.B * H;
         const int grid_p = pairs < num_sms() ? pairs : num_sms();
-        k_attn_tp<<<grid_p, TpCfg::THREADS, TpCfg::SMEM, s>>>(mk, mv, a);
-        return cudaGetLastError();
+        return launch(k_attn_tp, dim3(grid_p), dim3(TpCfg::THREADS), TpCfg::SMEM, s, mk, mv, a);
     }
     dim3 grid(plan.splits, H, t.B);
     return v.launch(grid, mk, mv, a, s);

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) k_attn_f32(float *out, const float *q, co
     constexpr int PER = D / 32;
     const int h = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b], P = prefix_len[b];
     if (n <= 0) return;
     if (P < 0 || P + n > L_max) {
@@ -72,10 +74,10 @@ cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, co
                             uint32_t *status, cudaStream_t s) {
     dim3 grid(H, t.B);
     if (d == 64)
-        k_attn_f32<64><<<grid, 256, 0, s>>>(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, status);
-    else
-        k_attn_f32<128><<<grid, 256, 0, s>>>(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, status);
-    return cudaGetLastError();
+        return launch(k_attn_f32<64>, grid, dim3(256), 0, s, out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale,
+                      status);
+    return launch(k_attn_f32<128>, grid, dim3(256), 0, s, out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale,
+                  status);
 }
 
 }  // namespace ts

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 
                                                           const uint4 *v_new, const int32_t *prefix_len, ts_tree t,
                                                           int H, int row_vec, int L_max, uint32_t *status) {
     const int b = blockIdx.y, h = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b], P = prefix_len[b];
     if (n <= 0) return;
     if (P < 0 || P + n > L_max) {
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 
                                                           const int32_t *out_count, ts_tree t, int H, int row_vec,
                                                           int L_max, uint32_t *status) {
     const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b], P = prefix_len[b];
     const int cnt = out_count[b];
     __shared__ int src_s[kMaxNodes + 1];
@@ -113,9 +117,8 @@ cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, co
                              uint32_t *status, cudaStream_t s) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
-    k_kv_append<<<grid, kKvThreads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new,
-                                     (const uint4 *)v_new, prefix_len, t, H, row_vec, L_max, status);
-    return cudaGetLastError();
+    return launch(k_kv_append, grid, dim3(kKvThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new,
+                  (const uint4 *)v_new, prefix_len, t, H, row_vec, L_max, status);
 }
 
 cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int32_t *new_prefix_len,
@@ -123,9 +126,8 @@ cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix
                              int L_max, int esize, uint32_t *status, cudaStream_t s) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
-    k_kv_commit<<<grid, kKvThreads, 0, s>>>((uint4 *)k_cache, (uint4 *)v_cache, prefix_len, new_prefix_len, out_path,
-                                    out_count, t, H, row_vec, L_max, status);
-    return cudaGetLastError();
+    return launch(k_kv_commit, grid, dim3(kKvThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, prefix_len,
+                  new_prefix_len, out_path, out_count, t, H, row_vec, L_max, status);
 }
 
 }  // namespace ts

@@ -127,6 +127,8 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_parent(ts_tree t, const int
     __shared__ Smem sm;
     const int b = blockIdx.x, v = threadIdx.x;
     const int n = n_nodes[b];
+    pdl_wait();
+    pdl_trigger();
     const int P = prefix_len ? prefix_len[b] : 0;
     if (n < 1 || n > t.n_max) {
         __syncthreads();
@@ -147,6 +149,8 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int
     __shared__ Smem sm;
     const int b = blockIdx.x, v = threadIdx.x;
     const int n = w.n;
+    pdl_wait();
+    pdl_trigger();
     const int P = prefix_len ? prefix_len[b] : 0;
     if (v < n) {
         int p = -1;
@@ -173,6 +177,8 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_chains(ts_tree t, const int
     __shared__ int canon[kMaxNodes];
     __shared__ int n_sh;
     const int b = blockIdx.x, s = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int S = C * len;
     const int32_t *ch = chains + (size_t)b * S;
     const int P = prefix_len ? prefix_len[b] : 0;
@@ -231,22 +237,19 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_chains(ts_tree t, const int
 cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
                                      const int32_t *n_nodes, const int32_t *prefix_len, uint32_t *status,
                                      cudaStream_t s) {
-    k_build_parent<<<t.B, kMaxNodes, 0, s>>>(t, tokens, parent, n_nodes, prefix_len, status);
-    return cudaGetLastError();
+    return launch(k_build_parent, dim3(t.B), dim3(kMaxNodes), 0, s, t, tokens, parent, n_nodes, prefix_len, status);
 }
 
 cudaError_t launch_tree_build_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
-    k_build_widths<<<t.B, kMaxNodes, 0, s>>>(t, tokens, w, prefix_len, status);
-    return cudaGetLastError();
+    return launch(k_build_widths, dim3(t.B), dim3(kMaxNodes), 0, s, t, tokens, w, prefix_len, status);
 }
 
 cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token, const int32_t *chains, int C,
                                      int len, int32_t *tokens_out, int32_t *p_row, int32_t *q_row,
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
-    k_build_chains<<<t.B, kMaxNodes, 0, s>>>(t, root_token, chains, C, len, tokens_out, p_row, q_row,
-                                             prefix_len, status);
-    return cudaGetLastError();
+    return launch(k_build_chains, dim3(t.B), dim3(kMaxNodes), 0, s, t, root_token, chains, C, len, tokens_out, p_row,
+                  q_row, prefix_len, status);
 }
 
 }  // namespace ts

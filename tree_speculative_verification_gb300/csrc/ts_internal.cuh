@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/treespec.h"
 
 namespace ts {
@@ -16,6 +18,33 @@ constexpr long long kWaitCycles = 4000000000LL;
 
 __device__ __forceinline__ void flag(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may be scheduled while the kernel before it on the stream
+// is still running, and pdl_wait() -- the first thing each kernel does before
+// it reads or writes global memory -- blocks until that kernel has completed
+// and its writes are visible. pdl_trigger() lets the next kernel be scheduled
+// early. Both are no-ops without a programmatic neighbour.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+bool pdl_enabled();   // false when TREESPEC_PDL=0
+
+template <typename... K, typename... A>
+cudaError_t launch(void (*kern)(K...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 
 // ---- launchers (one per .cu file) -------------------------------------------
@@ -48,6 +77,8 @@ struct AttnPlan {
     int chunk_tiles;   // 64-key tiles per CTA
     int n_pad;         // node rows kept per partial
     size_t ws_bytes;   // partials + counters
+    bool persistent;   // the persistent tcgen05 kernel walks the (b, h) items
+    const char *kernel;  // name of the kernel the launch uses
 };
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
 

@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
                                                            uint32_t *status) {
     const int b = blockIdx.y;
     const int v = blockIdx.x / seg, sg = blockIdx.x % seg;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b];
     const int n_max = t.n_max;
     if (n <= 0) {
@@ -318,6 +320,8 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
     MssShared &sm = *reinterpret_cast<MssShared *>(smem_raw);
     float *Rs = SMEM_R ? reinterpret_cast<float *>(smem_raw + kMssHeader) : nullptr;
     const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int n = t.n_nodes[b];
     const int n_max = t.n_max;
     int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
@@ -666,9 +670,8 @@ cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t
     unsigned *counters = (unsigned *)ws;
     ArgPart *parts = (ArgPart *)((char *)ws + ((size_t)t.B * sizeof(unsigned) + 255) / 256 * 256);
     dim3 grid(t.n_max * seg, t.B);
-    k_greedy<<<grid, kGreedyThreads, 0, s>>>(out_tokens, out_path, out_count, argmax_out, logits, t, V, seg, vec4,
-                                             counters, parts, status);
-    return cudaGetLastError();
+    return launch(k_greedy, grid, dim3(kGreedyThreads), 0, s, out_tokens, out_path, out_count, argmax_out, logits, t,
+                  V, seg, vec4, counters, parts, status);
 }
 
 cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
@@ -682,13 +685,11 @@ cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *o
     if (with_row <= (size_t)optin) {
         cudaError_t e = cudaFuncSetAttribute(k_mss<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_row);
         if (e != cudaSuccess) return e;
-        k_mss<true><<<t.B, kMssThreads, with_row, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row,
-                                                      NQ, uniforms, 1.0f / temperature, t, V, status);
-    } else {
-        k_mss<false><<<t.B, kMssThreads, kMssHeader, s>>>(out_tokens, out_path, out_count, logits, p_row, NP, ssm,
-                                                         q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+        return launch(k_mss<true>, dim3(t.B), dim3(kMssThreads), with_row, s, out_tokens, out_path, out_count, logits,
+                      p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
     }
-    return cudaGetLastError();
+    return launch(k_mss<false>, dim3(t.B), dim3(kMssThreads), (size_t)kMssHeader, s, out_tokens, out_path, out_count,
+                  logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
 }
 
 }  // namespace ts
