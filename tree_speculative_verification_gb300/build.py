@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreespec.so")
-SOURCES = ["api.cu", "tree_build.cu", "kv.cu", "attn_f32.cu", "attn_bf16.cu", "verify.cu", "attn_noalloc.cu"]
+SOURCES = ["api.cu", "tree_build.cu", "kv.cu", "attn_f32.cu", "attn_bf16.cu", "attn_kt.cu", "verify.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -48,8 +48,8 @@ def _digest(files) -> str:
 def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
     """Compile every CUDA source and link libtreespec.so; returns its path.
     Rebuilds only when a source or header changed (or force)."""
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "ts_internal.cuh"),
-                                                       os.path.join(ROOT, "include", "treespec.h")]
+    headers = sorted(f for f in os.listdir(CSRC) if f.endswith(".cuh"))
+    deps = [os.path.join(CSRC, s) for s in SOURCES + headers] + [os.path.join(ROOT, "include", "treespec.h")]
     stamp = os.path.join(BUILD, "stamp")
     digest = _digest(deps)
     if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == digest:

@@ -25,6 +25,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include "attn_common.cuh"
 #include "ts_internal.cuh"
 
 namespace ts {
@@ -60,56 +61,6 @@ struct Cfg {
 };
 
 // ------------------------------------------------------------ PTX helpers ---
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(phase)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bounded wait: false after kWaitCycles without completion.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase);
-// The same wait taken by a whole warp, with one verdict for every lane, so that
-// warp-collective instructions after it are never reached by only part of it.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t phase) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, phase));
-}
-
-// Bounded wait: false after kWaitCycles without completion.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase) {
-    if (mbar_try_wait(bar, phase)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, phase))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -137,32 +88,7 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &lo_r, float &hi_r) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    lo_r = __bfloat162float(v.x);
-    hi_r = __bfloat162float(v.y);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// 128-byte-swizzled byte offset of (row, 16-byte chunk) inside a TMA box.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 // ---------------------------------------------------------------- kernel ----
-struct AttnArgs {
-    __nv_bfloat16 *out;
-    const __nv_bfloat16 *q;
-    const int32_t *prefix_len;
-    ts_tree t;
-    int H, L_max;
-    float scale_log2;
-    int chunk_tiles, splits, n_pad;
-    unsigned *counters;
-    float *part_ml;   // [B*H*splits][2][n_pad]
-    float *part_o;    // [B*H*splits][n_pad][D]
-    uint32_t *status;
-};
 
 // After a CTA has published its partial (max, sum, unnormalised O) for key
 // split sidx of (b, h), the CTA that arrives last on the (b, h) counter merges
@@ -611,50 +537,6 @@ struct TcCfg {
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;            // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
 };
-
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;   // descriptor version of the sm_100 family
-    d |= (uint64_t)2 << 61;   // 128-byte swizzle
-    return d;
-}
-
-// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, A K-major.
-constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
-                 : "r"(taddr));
-}
-
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-                 :: "r"(taddr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
-                 : "memory");
-}
 
 __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_constant__ CUtensorMap map_k,
                                                                const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
@@ -1404,34 +1286,6 @@ __global__ void __launch_bounds__(TpCfg::THREADS, 1) k_attn_tp(const __grid_cons
 }
 
 // ------------------------------------------------------------------ host ----
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)p;
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap *map, const void *base, int d, long long rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    cuuint32_t box[2] = {64, TK};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 struct Variant {
     int nodes, threads, smem;
@@ -1474,11 +1328,20 @@ cudaError_t launch_tc(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, c
     return launch(k_attn_tc, grid, dim3(TcCfg::THREADS), TcCfg::SMEM, s, mk, mv, a);
 }
 
-// Kernel choice: the tcgen05 kernel for head_dim 128 and trees of at most 128
-// nodes unless TREESPEC_ATTN_KERNEL=mma asks for the mma.sync kernel.
-// Measured on GB300: for trees of up to 32 nodes the mma.sync kernel wins
-// (only one softmax warp of the tcgen05 kernel has rows to work on); from 33
-// nodes on, the tcgen05 kernel's tensor-core throughput wins.
+// Kernel choice for head_dim 128: trees of 33..128 nodes go to the 128-row
+// tcgen05 kernel, all others (and head_dim 64) to the mma.sync kernel.
+// TREESPEC_ATTN_KERNEL=mma, tc or kt forces one of them where its limits
+// allow; kt is the small-tree tcgen05 kernel (at most 32 nodes, keys on the
+// MMA's M side, key tiles cut evenly over the SMs). Measured on GB300 for a
+// 21-node tree over a 2048-key prefix (batch 8, 32 heads): mma.sync 58 us,
+// kt 81-84 us -- one CTA per SM exposes kt's startup, per-pair epilogues and
+// merges, which the mma.sync kernel's two CTAs per SM overlap.
+bool use_kt(int d, int n_max) {
+    if (d != 128 || n_max > 32) return false;
+    const char *e = getenv("TREESPEC_ATTN_KERNEL");
+    return e && strcmp(e, "kt") == 0;
+}
+
 bool use_tc(int d, int n_max) {
     if (d != 128 || n_max > TcCfg::NODES) return false;
     const char *e = getenv("TREESPEC_ATTN_KERNEL");
@@ -1515,8 +1378,15 @@ int num_sms() {
 }
 
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
-    AttnPlan p{1, 1, 0, 0, false, "k_attn_f32"};
+    AttnPlan p{1, 1, 0, 0, false, false, "k_attn_f32"};
     if (dt != TS_BF16) return p;
+    if (use_kt(d, n_max)) {
+        p.n_pad = 32;
+        p.small_tree = true;
+        p.kernel = "k_attn_kt";
+        p.ws_bytes = attn_kt_ws_bytes(B, H);
+        return p;
+    }
     const Variant v = pick_variant(d, n_max);
     p.kernel = v.name;
     const int tiles = (L_max + TK - 1) / TK;
@@ -1550,10 +1420,12 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max, float scale,
                              const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s, const char **why) {
+    if (plan.small_tree)
+        return launch_attn_kt(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, ws, status, s, why);
     const Variant v = pick_variant(d, t.n_max);
     CUtensorMap mk, mv;
     const long long rows = (long long)t.B * H * L_max;
-    if (!make_map(&mk, k_cache, d, rows) || !make_map(&mv, v_cache, d, rows)) {
+    if (!make_map(&mk, k_cache, d, rows, TK) || !make_map(&mv, v_cache, d, rows, TK)) {
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
     }

@@ -78,6 +78,7 @@ struct AttnPlan {
     int n_pad;         // node rows kept per partial
     size_t ws_bytes;   // partials + counters
     bool persistent;   // the persistent tcgen05 kernel walks the (b, h) items
+    bool small_tree;   // the small-tree tcgen05 kernel (key tiles cut evenly over the SMs)
     const char *kernel;  // name of the kernel the launch uses
 };
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
@@ -85,6 +86,12 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
 cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, const float *v_cache,
                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                             float scale, uint32_t *status, cudaStream_t s);
+// Small-tree tcgen05 kernel (head_dim 128, at most 32 nodes): workspace bytes
+// and launch.
+size_t attn_kt_ws_bytes(int B, int H);
+cudaError_t launch_attn_kt(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale, void *ws,
+                           uint32_t *status, cudaStream_t s, const char **why);
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,
