@@ -106,24 +106,60 @@ __device__ void merge_splits(const AttnArgs &a, int b, int h, int n, int S_b, co
     if (!flag_s[0]) return;
     __threadfence();
     const int n_max = a.t.n_max;
-    for (int idx = tid; idx < n * (D / 2); idx += nthreads) {
-        const int i = idx / (D / 2), dp = (idx % (D / 2)) * 2;
-        float M = -INFINITY;
-        for (int s = 0; s < S_b; ++s) M = fmaxf(M, __ldcg(a.part_ml + (bh * a.splits + s) * 2 * a.n_pad + i));
-        float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
-        for (int s = 0; s < S_b; ++s) {
-            const float *pml = a.part_ml + (bh * a.splits + s) * 2 * a.n_pad;
-            const float ms = __ldcg(pml + i);
-            if (ms == -INFINITY) continue;
-            const float f = exp2f(ms - M);
-            Lsum += __ldcg(pml + a.n_pad + i) * f;
-            const float2 ov = __ldcg((const float2 *)(a.part_o + ((bh * a.splits + s) * a.n_pad + i) * D + dp));
-            o0 += ov.x * f;
-            o1 += ov.y * f;
+    // Each thread merges up to four (node, dim pair) items at a time, four splits
+    // at a time, with every load of a group issued before any is used.
+    constexpr int IT = 4, SG = 4;
+    const int items = n * (D / 2);
+    for (int idx0 = tid; idx0 < items; idx0 += IT * nthreads) {
+        float M[IT], Ls[IT], o0[IT], o1[IT];
+        int ii[IT], dd[IT];
+#pragma unroll
+        for (int q = 0; q < IT; ++q) {
+            const int idx = idx0 + q * nthreads;
+            ii[q] = idx < items ? idx / (D / 2) : -1;
+            dd[q] = idx < items ? (idx % (D / 2)) * 2 : 0;
+            M[q] = -INFINITY;
+            Ls[q] = o0[q] = o1[q] = 0.f;
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        *(__nv_bfloat162 *)(a.out + (((size_t)b * n_max + perm_s[i]) * a.H + h) * D + dp) =
-            __floats2bfloat162_rn(o0 * inv, o1 * inv);
+        for (int s0 = 0; s0 < S_b; s0 += SG) {
+            float ms[IT][SG], ls[IT][SG];
+            float2 ov[IT][SG];
+#pragma unroll
+            for (int q = 0; q < IT; ++q)
+#pragma unroll
+                for (int k = 0; k < SG; ++k) {
+                    const int sp = s0 + k;
+                    if (ii[q] >= 0 && sp < S_b) {
+                        const float *pml = a.part_ml + (bh * a.splits + sp) * 2 * a.n_pad;
+                        ms[q][k] = __ldcg(pml + ii[q]);
+                        ls[q][k] = __ldcg(pml + a.n_pad + ii[q]);
+                        ov[q][k] = __ldcg((const float2 *)(a.part_o + ((bh * a.splits + sp) * a.n_pad + ii[q]) * D + dd[q]));
+                    } else {
+                        ms[q][k] = -INFINITY;
+                        ls[q][k] = 0.f;
+                        ov[q][k] = make_float2(0.f, 0.f);
+                    }
+                }
+#pragma unroll
+            for (int q = 0; q < IT; ++q)
+#pragma unroll
+                for (int k = 0; k < SG; ++k) {
+                    const float mn = fmaxf(M[q], ms[q][k]);
+                    const float fo = M[q] == mn ? 1.f : exp2f(M[q] - mn);   // 0 from -inf
+                    const float fs = ms[q][k] == mn ? 1.f : exp2f(ms[q][k] - mn);
+                    Ls[q] = Ls[q] * fo + ls[q][k] * fs;
+                    o0[q] = o0[q] * fo + ov[q][k].x * fs;
+                    o1[q] = o1[q] * fo + ov[q][k].y * fs;
+                    M[q] = mn;
+                }
+        }
+#pragma unroll
+        for (int q = 0; q < IT; ++q)
+            if (ii[q] >= 0) {
+                const float inv = Ls[q] > 0.f ? 1.f / Ls[q] : 0.f;
+                *(__nv_bfloat162 *)(a.out + (((size_t)b * n_max + perm_s[ii[q]]) * a.H + h) * D + dd[q]) =
+                    __floats2bfloat162_rn(o0[q] * inv, o1[q] * inv);
+            }
     }
     if (tid == 0) a.counters[bh] = 0u;   // leave the workspace zeroed
 }
@@ -142,7 +178,7 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp / KS, ks = warp % KS;
     const int g = lane >> 2, tq = lane & 3;
-    const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
+    const int b = blockIdx.y, h = blockIdx.x, sidx = blockIdx.z;
     const ts_tree &t = a.t;
     pdl_wait();
     pdl_trigger();
@@ -551,7 +587,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout, [2] merge flag
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, h = blockIdx.y, sidx = blockIdx.x;
+    const int b = blockIdx.y, h = blockIdx.x, sidx = blockIdx.z;
     const ts_tree &t = a.t;
     pdl_wait();
     pdl_trigger();
@@ -1393,15 +1429,20 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
     const long long pairs = (long long)B * H;
     const long long slots = (long long)num_sms() * occupancy(v);
     // Split the key axis only when the (request, head) pairs fill at most half
-    // a wave of CTA slots: every split costs a prologue and a partial write, and
-    // splitting 256 pairs over 304 slots measured 1.7x slower than not.
-    int splits = 1;
-    if (2 * pairs <= slots) splits = (int)((slots + pairs - 1) / pairs);
-    if (const char *e = getenv("TREESPEC_ATTN_SPLITS"))
-        if (*e) splits = atoi(e);
-    splits = splits < 1 ? 1 : (splits > kMaxSplits ? kMaxSplits : splits);
-    splits = splits > tiles ? tiles : splits;
-    p.chunk_tiles = (tiles + splits - 1) / splits;
+    // a wave of CTA slots, into equal chunks. Measured on GB300 (llama7b layer,
+    // 256 pairs of 33 tiles on 304 slots): no split 58 us; two equal chunks
+    // 1.7x slower; chunks of 28 and 5 tiles dispatched longest-first 71 us.
+    long long chunk = tiles;
+    if (2 * pairs <= slots) chunk = (tiles + (slots + pairs - 1) / pairs - 1) / ((slots + pairs - 1) / pairs);
+    if (const char *e = getenv("TREESPEC_ATTN_SPLITS"))   // equal chunks, this many
+        if (*e) {
+            int sp = atoi(e);
+            sp = sp < 1 ? 1 : (sp > tiles ? tiles : sp);
+            chunk = (tiles + sp - 1) / sp;
+        }
+    const long long min_chunk = (tiles + kMaxSplits - 1) / kMaxSplits;
+    if (chunk < min_chunk) chunk = min_chunk;
+    p.chunk_tiles = (int)chunk;
     p.splits = (tiles + p.chunk_tiles - 1) / p.chunk_tiles;
     p.n_pad = v.nodes;
     const size_t counters = ((size_t)pairs * 4 + 255) / 256 * 256;
@@ -1455,7 +1496,8 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
         const int grid_p = pairs < num_sms() ? pairs : num_sms();
         return launch(k_attn_tp, dim3(grid_p), dim3(TpCfg::THREADS), TpCfg::SMEM, s, mk, mv, a);
     }
-    dim3 grid(plan.splits, H, t.B);
+    // split index slowest: every first (longest) chunk is dispatched before any later one
+    dim3 grid(H, t.B, plan.splits);
     return v.launch(grid, mk, mv, a, s);
 }
 
