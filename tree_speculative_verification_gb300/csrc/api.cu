@@ -105,6 +105,8 @@ ts_status tree_build(const ts_tree *t, const int32_t *tokens, const int32_t *par
             w.level_start[l + 2] = (int)n;
         }
         w.n = (int)n;
+        w.sub[m] = 1;
+        for (int l = m - 1; l >= 0; --l) w.sub[l] = 1 + w.width[l] * w.sub[l + 1];
         return cuda_result(ts::launch_tree_build_widths(*t, tokens, w, prefix_len, status, stream), "tree_build");
     }
     if (!parent || !n_nodes) return fail(TS_ERR_INVALID_ARG, "tree_build: parent mode needs parent and n_nodes");

@@ -144,24 +144,63 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_parent(ts_tree t, const int
     linearize(t, b, n, sm, P, status);
 }
 
+// Expansion trees (sec. 3, Fig. 3): every node at depth d has width[d]
+// children, numbered level by level, so a node's place in depth-first order is
+// mixed-radix arithmetic on the subtree sizes sub[]: thread i takes
+// depth-first position i, walks down from the root choosing child
+// (rest - 1) / sub[d + 1] at each depth, and gets its input id, depth, parent,
+// subtree end and ancestors without shared memory or barriers.
 __global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int32_t *tokens, WidthsParam w,
                                                             const int32_t *prefix_len, uint32_t *status) {
-    __shared__ Smem sm;
-    const int b = blockIdx.x, v = threadIdx.x;
-    const int n = w.n;
+    const int b = blockIdx.x, i = threadIdx.x;
+    const int n = w.n, n_max = t.n_max, W = TS_MASK_WORDS(n_max);
     pdl_wait();
     pdl_trigger();
     const int P = prefix_len ? prefix_len[b] : 0;
-    if (v < n) {
-        int p = -1;
-        for (int l = 1; l <= w.m; ++l)
-            if (v >= w.level_start[l] && v < w.level_start[l + 1])
-                p = w.level_start[l - 1] + (v - w.level_start[l]) / w.width[l - 1];
-        sm.par[v] = p;
-        sm.tok[v] = tokens[(size_t)b * t.n_max + v];
+    const size_t o = (size_t)b * n_max + i;
+    if (i < n) {
+        int d = 0, pos = 0, par = -1, idx = 0;   // current node: depth, DFS position, parent position, index in level
+        int rest = i;                            // DFS offset of the target inside the current subtree
+        int path[17];                            // DFS positions on the root path
+        path[0] = 0;
+#pragma unroll
+        for (int l = 0; l < 16; ++l)
+            if (l < w.m && rest > 0) {
+                const int c = (rest - 1) / w.sub[l + 1];
+                par = pos;
+                pos = pos + 1 + c * w.sub[l + 1];
+                rest = rest - 1 - c * w.sub[l + 1];
+                idx = idx * w.width[l] + c;
+                d = l + 1;
+                path[d] = pos;
+            }
+        const int v = w.level_start[d] + idx;
+        t.perm[o] = v;
+        t.dfs_of[(size_t)b * n_max + v] = i;
+        t.parent[o] = par;
+        t.token[o] = tokens[(size_t)b * n_max + v];
+        t.depth[o] = d;
+        if (t.pos) t.pos[o] = P + d;
+        t.sub_end[o] = i + w.sub[d];
+        for (int wd = 0; wd < W; ++wd) {
+            uint32_t bits = 0u;
+#pragma unroll
+            for (int l = 0; l <= 16; ++l)
+                if (l <= d && (path[l] >> 5) == wd) bits |= 1u << (path[l] & 31);
+            t.anc[o * W + wd] = bits;
+        }
+    } else if (i < n_max) {
+        t.perm[o] = -1;
+        t.dfs_of[o] = -1;
+        t.parent[o] = -1;
+        t.token[o] = -1;
+        t.depth[o] = -1;
+        if (t.pos) t.pos[o] = -1;
+        t.sub_end[o] = -1;
+        for (int wd = 0; wd < W; ++wd) t.anc[o * W + wd] = 0u;
     }
-    __syncthreads();
-    linearize(t, b, n, sm, P, status);
+    if (i == 0) t.n_nodes[b] = n;
+    (void)status;
 }
 
 // Def. 3.2 merge, data-parallel: slot s = (chain c, position p). The slot

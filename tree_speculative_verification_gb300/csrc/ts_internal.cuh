@@ -53,6 +53,7 @@ struct WidthsParam {
     int n;                 // total node count
     int level_start[17];   // start id of each level, level_start[m+1] = n
     int width[16];
+    int sub[17];           // size of a subtree rooted at depth d (sub[m] = 1)
 };
 
 cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
