@@ -416,8 +416,9 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                 }
             }
         }
-        if (block_or(sm, nf)) { nonfinite = 1; break; }
-        const float m = block_max(sm, mx);
+        // one reduction for both: a non-finite logit makes the maximum +inf
+        const float m = block_max(sm, nf ? INFINITY : mx);
+        if (m == INFINITY) { nonfinite = 1; break; }
         // pass 2: e = 2^((l/T - m) log2 e) and Z = sum e
         float s = 0.f, cc = 0.f;
         if (SMEM_R) {
@@ -514,8 +515,9 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                     kahan(s2, c2, fmaxf(0.f, __fmaf_rn(-Sf, qy, resid_recompute(rr, y))));
                 }
             }
-            if (block_or(sm, bad)) { nonfinite = 1; break; }
-            const double Snew = block_sum(sm, s2, -c2);
+            // one reduction for both: a non-finite drafter value makes the sum NaN
+            const double Snew = block_sum(sm, bad ? NAN : s2, bad ? 0.f : -c2);
+            if (isnan(Snew)) { nonfinite = 1; break; }
             if (Snew > 0.0) {
                 if (tid == 0) {
                     sm.rej_q[nrej] = qc;
