@@ -202,26 +202,6 @@ def _events(n, external):
     return [torch.cuda.Event(**kw) for _ in range(n)]
 
 
-def enqueue_steps(s, kind, K, ev, stream, att=None, ver=None):
-    """K verification steps on `stream` between the events ev[0], ev[1]; with
-    `att`/`ver`, also events around each step's attention and verify launches."""
-    ev[0].record(stream)
-    for i in range(K):
-        s.build()
-        s.append()
-        if att is not None:
-            att[2 * i].record(stream)
-        s.attend()
-        if att is not None:
-            att[2 * i + 1].record(stream)
-            ver[2 * i].record(stream)
-        s.verify(kind)
-        if ver is not None:
-            ver[2 * i + 1].record(stream)
-        s.commit(kind)
-    ev[1].record(stream)
-
-
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -286,49 +266,53 @@ def run_ours(args):
 
     # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream).
     # The K steps are captured once into a CUDA graph (each step is the same five
-    # library calls; the graph removes the host launch overhead between them).
-    # The timed pass has events at its two ends only: an event-record node
-    # between two kernels of a graph costs a few microseconds. A second timed
-    # pass of the same K steps, captured with event nodes around every
-    # attention and verify launch, gives those kernels' durations.
+    # library calls; the graph removes the host launch overhead between them),
+    # with events at its two ends only: an event-record node between two kernels
+    # of a graph costs a few microseconds. The attention and verify durations
+    # come from two more timed passes, each a graph of K back-to-back launches of
+    # that one call on the same inputs (events at the ends; the time between two
+    # launches counts, so the figure is conservative).
     for _ in range(args.warmup):
         s.run(kind)
     torch.cuda.synchronize()
     K = args.steps
+    passes = {
+        "step": lambda cur: [s.run(kind) for _ in range(K)],
+        "attend": lambda cur: [s.attend() for _ in range(K)],
+        "verify": lambda cur: [s.verify(kind) for _ in range(K)],
+    }
+    evs = {k: _events(2, not args.eager) for k in passes}
     graphs, launch_mode = None, "eager launches"
-    ev, ev2, att, ver = (_events(2, not args.eager), _events(2, not args.eager), _events(2 * K, not args.eager),
-                         _events(2 * K, not args.eager))
     if not args.eager:
         try:
-            graphs = []
-            for with_kernel_events in (False, True):
+            graphs = {}
+            for k, body in passes.items():
                 g = torch.cuda.CUDAGraph()
                 cs = torch.cuda.Stream(device)
                 cs.wait_stream(stream)
                 with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
                     cur = torch.cuda.current_stream(device)
-                    if with_kernel_events:
-                        enqueue_steps(s, kind, K, ev2, cur, att, ver)
-                    else:
-                        enqueue_steps(s, kind, K, ev, cur)
+                    evs[k][0].record(cur)
+                    body(cur)
+                    evs[k][1].record(cur)
                 stream.wait_stream(cs)
                 g.replay()
                 torch.cuda.synchronize()
-                graphs.append(g)
+                graphs[k] = g
             launch_mode = "CUDA graph of the K steps"
         except Exception as exc:     # no graph support for event nodes: time eager launches
             graphs = None
             launch_mode = f"eager launches ({type(exc).__name__} capturing a graph)"
             torch.cuda.synchronize()
-            ev, ev2, att, ver = _events(2, False), _events(2, False), _events(2 * K, False), _events(2 * K, False)
+            evs = {k: _events(2, False) for k in passes}
 
-    def timed_pass(with_kernel_events=False):
+    def timed_pass(k="step"):
         if graphs is not None:
-            graphs[1 if with_kernel_events else 0].replay()
-        elif with_kernel_events:
-            enqueue_steps(s, kind, K, ev2, stream, att, ver)
+            graphs[k].replay()
         else:
-            enqueue_steps(s, kind, K, ev, stream)
+            evs[k][0].record(stream)
+            passes[k](stream)
+            evs[k][1].record(stream)
 
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
     t_load0 = time.time()
@@ -342,7 +326,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     t_wall1 = time.time()
-    timed_pass(with_kernel_events=True)
+    ms = evs["step"][0].elapsed_time(evs["step"][1])
+    timed_pass("attend")
+    timed_pass("verify")
     torch.cuda.synchronize()
     t_load1 = time.time()
     while time.time() - t_load1 < 0.4:
@@ -350,10 +336,8 @@ def run_ours(args):
         torch.cuda.synchronize()
     if sampler:
         sampler.stop()
-    ms = ev[0].elapsed_time(ev[1])
-    ms_kernel_events = ev2[0].elapsed_time(ev2[1])
-    t_att = sum(att[2 * i].elapsed_time(att[2 * i + 1]) for i in range(K)) / K
-    t_ver = sum(ver[2 * i].elapsed_time(ver[2 * i + 1]) for i in range(K)) / K
+    t_att = evs["attend"][0].elapsed_time(evs["attend"][1]) / K
+    t_ver = evs["verify"][0].elapsed_time(evs["verify"][1]) / K
     if dist:
         tt = torch.tensor([ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -391,11 +375,11 @@ def run_ours(args):
                        "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
                        "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "launch": launch_mode,
-                       "kernel_timing": "attention and verify durations from a second timed pass of the same "
-                                        "K steps with event nodes around each of their launches",
+                       "kernel_timing": "attention and verify durations from graphs of K back-to-back launches "
+                                        "of that call on the same inputs, events at both ends",
                        "l2": f"inputs larger than L2: {abytes / 2**20:.0f} MiB of K/V+Q per step vs 129 MiB"},
             "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
-            "attention_ms": t_att, "verify_ms": t_ver, "ms_per_step_with_kernel_events": ms_kernel_events / args.steps,
+            "attention_ms": t_att, "verify_ms": t_ver,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": args.steps * s.launches_per_step(kind)}
     print(json.dumps(line), flush=True)

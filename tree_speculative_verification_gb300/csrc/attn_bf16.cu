@@ -32,12 +32,18 @@ namespace ts {
 namespace {
 
 constexpr int TK = 64;       // keys per pipeline tile
-constexpr int STAGES = 3;
 constexpr int kMaxSplits = 64;
 
-template <int D_, int NT_, int NG_, int KS_>
+// STG_: TMA ring stages; QR_: Q fragments held in registers for the whole pass
+// (else re-read from shared memory per k-step pair, 48 registers fewer at 24
+// nodes); MINB_: CTAs per SM the register allocation must allow. Measured on
+// GB300 (21 nodes, 2048-key prefix, 256 pairs): <3, regs, 1> 50.7 us,
+// <3, smem, 2> 51.0, <2, regs, 2> 52.5, <2, smem, 2> 53.0, <2, smem, 3> with
+// three CTAs per SM 58.8 -- more warps per SM do not help this kernel.
+template <int D_, int NT_, int NG_, int KS_, int STG_ = 3, bool QR_ = true, int MINB_ = 1>
 struct Cfg {
-    static constexpr int D = D_, NT = NT_, NG = NG_, KS = KS_;
+    static constexpr int D = D_, NT = NT_, NG = NG_, KS = KS_, STG = STG_, MINB = MINB_;
+    static constexpr bool QR = QR_;
     static constexpr int WARPS = NG * KS, THREADS = WARPS * 32;
     static constexpr int NODES = NG * NT * 8;            // node columns held (padded)
     static constexpr int BOXES = D / 64;                  // 64-column (128-byte) TMA boxes per row
@@ -50,13 +56,13 @@ struct Cfg {
     static constexpr int ANC_BYTES = NODES * kMaxWords * 4;
     static constexpr int NT8P = NT * 8 + 4;               // padded node stride of the merge slots
     static constexpr int SLOT_FLOATS = 2 * NT * 8 + D * NT8P;
-    static constexpr int OFF_Q = STAGES * STAGE_BYTES;
+    static constexpr int OFF_Q = STG * STAGE_BYTES;
     static constexpr int OFF_ANC = OFF_Q + Q_BYTES;
     static constexpr int OFF_PERM = OFF_ANC + ANC_BYTES;
     static constexpr int OFF_BAR = OFF_PERM + NODES * 4;
-    static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int OFF_MISC = OFF_BAR + 2 * STG * 8;
     static constexpr int SMEM = OFF_MISC + 16 + 1024;     // + slack for 1024-byte alignment
-    static_assert(NG * (KS - 1) * SLOT_FLOATS * 4 <= STAGES * STAGE_BYTES, "merge slots exceed stage memory");
+    static_assert(NG * (KS - 1) * SLOT_FLOATS * 4 <= STG * STAGE_BYTES, "merge slots exceed stage memory");
     static_assert(KEYS_PER_WARP % 16 == 0, "warp key slice must be a multiple of 16");
 };
 
@@ -165,9 +171,10 @@ __device__ void merge_splits(const AttnArgs &a, int b, int h, int n, int S_b, co
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant__ CUtensorMap map_k,
-                                                          const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
-    constexpr int D = C::D, NT = C::NT, KS = C::KS;
+__global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_constant__ CUtensorMap map_k,
+                                                                   const __grid_constant__ CUtensorMap map_v,
+                                                                   AttnArgs a) {
+    constexpr int D = C::D, NT = C::NT, KS = C::KS, STAGES = C::STG;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sm_base = smem_u32(sm);
@@ -243,20 +250,22 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
     }
     __syncthreads();
 
-    // Q as B operand fragments, held in registers for the whole pass
+    // Q as B operand fragments: for k-step pair (kk, kk + 1) and node tile j,
+    // one ldmatrix.x4 from the swizzled Q rows; held in registers for the
+    // whole pass (QR) or re-read at every use
     const int node0 = grp * NT * 8;
-    uint32_t qf[NT][D / 16][2];
-    {
-        const uint32_t qbase = sm_base + C::OFF_Q;
+    const uint32_t qbase = sm_base + C::OFF_Q;
+    auto load_q = [&](int j, int kk, uint32_t &q0, uint32_t &q1, uint32_t &q2, uint32_t &q3) {
+        const int r = node0 + j * 8 + (lane & 7);
+        const int c = kk * 2 + (lane >> 3);
+        ldsm_x4(qbase + r * (D * 2) + ((c ^ (r & 7)) << 4), q0, q1, q2, q3);
+    };
+    uint32_t qf[C::QR ? NT : 1][C::QR ? D / 16 : 1][2];
+    if constexpr (C::QR) {
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int kk = 0; kk < D / 16; kk += 2) {
-                const int r = node0 + j * 8 + (lane & 7);
-                const int c = kk * 2 + (lane >> 3);
-                ldsm_x4(qbase + r * (D * 2) + ((c ^ (r & 7)) << 4), qf[j][kk][0], qf[j][kk][1], qf[j][kk + 1][0],
-                        qf[j][kk + 1][1]);
-            }
+            for (int kk = 0; kk < D / 16; kk += 2) load_q(j, kk, qf[j][kk][0], qf[j][kk][1], qf[j][kk + 1][0], qf[j][kk + 1][1]);
     }
 
     float oacc[D / 16][NT][4];
@@ -306,14 +315,24 @@ __global__ void __launch_bounds__(C::THREADS) k_attn_bf16(const __grid_constant_
             float sacc[NT][4];
 #pragma unroll
             for (int j = 0; j < NT; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+            uint32_t qp[C::QR ? 1 : NT][4];
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int r = kb + (lane & 7) + (((lane >> 3) & 1) << 3);
                 const int chn = 2 * (kk & 3) + (lane >> 4);
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4(kb_addr + (kk >> 2) * C::BOX_BYTES + swz(r, chn), a0, a1, a2, a3);
+                if constexpr (C::QR) {
 #pragma unroll
-                for (int j = 0; j < NT; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qf[j][kk][0], qf[j][kk][1]);
+                    for (int j = 0; j < NT; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qf[j][kk][0], qf[j][kk][1]);
+                } else {
+                    if ((kk & 1) == 0)
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) load_q(j, kk, qp[j][0], qp[j][1], qp[j][2], qp[j][3]);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+                        mma_bf16(sacc[j], a0, a1, a2, a3, qp[j][(kk & 1) * 2], qp[j][(kk & 1) * 2 + 1]);
+                }
             }
             // the mask is needed only where the chunk reaches the tree rows or the chunk end
             if (key0 + 16 > P || key0 + 16 > k_end) {
@@ -1338,7 +1357,12 @@ cudaError_t launch_cfg(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, 
 template <class C>
 const char *cfg_name() {
     static char buf[48];
-    static const bool once = (snprintf(buf, sizeof buf, "k_attn_bf16<%d,%d,%d,%d>", C::D, C::NT, C::NG, C::KS), true);
+    static const bool once =
+        (C::STG == 3 && C::QR && C::MINB == 1
+             ? snprintf(buf, sizeof buf, "k_attn_bf16<%d,%d,%d,%d>", C::D, C::NT, C::NG, C::KS)
+             : snprintf(buf, sizeof buf, "k_attn_bf16<%d,%d,%d,%d,%d,%d,%d>", C::D, C::NT, C::NG, C::KS, C::STG,
+                        (int)C::QR, C::MINB),
+         true);
     (void)once;
     return buf;
 }
