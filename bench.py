@@ -167,6 +167,9 @@ def run_oracle_sample(w, heads: int, verify: bool = True):
                                    nthreads=0)
     t1 = time.perf_counter()
     if verify:
+        if w.verify == "naive":
+            oracle.verify_naive(np.stack([w.logits[b][p_row[b]] for b in range(w.B)]) if p_row is not None
+                                else w.logits, parent, tokens, n_nodes, w.uniforms, w.temperature)
         if w.verify in ("greedy", "both"):
             oracle.verify_greedy(w.logits, parent, tokens, n_nodes)
         if w.verify in ("mss", "both"):
@@ -217,6 +220,8 @@ def run_reference(args):
         return
     from tree_speculative_verification_gb300 import workloads
     w = workloads.make(args.config)
+    if args.verify:
+        w.verify = args.verify
     w.n_nodes_dev = _oracle_tree(w)[2]
     per_step_budget = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -250,6 +255,10 @@ def run_ours(args):
     from tree_speculative_verification_gb300.step import DeviceStep
     api.load_library()
     w = workloads.make(args.config, scale_down=args.scale_down)
+    if args.verify:
+        if args.verify in ("mss", "both") and w.ssm is None:
+            raise SystemExit(f"--verify {args.verify}: the {args.config} workload has no drafter distributions")
+        w.verify = args.verify
     s = DeviceStep(w, device)
     stream = torch.cuda.current_stream(device)
     kind = w.verify
@@ -257,6 +266,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     w.n_nodes_dev = s.tree.n_nodes.cpu().numpy()
     nodes_per_step = int(w.n_nodes_dev.sum())
+    accepted_per_step = s.accepted(kind)
     if s.status.item() not in (0, api.STATUS_ZERO_RESID):
         raise RuntimeError(f"device status {s.status.item()} after the first step")
 
@@ -381,6 +391,8 @@ def run_ours(args):
             "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
             "attention_ms": t_att, "verify_ms": t_ver,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "accepted_tokens_per_step": accepted_per_step,
+            "accepted_tokens_per_s": ws * accepted_per_step / (ms_per_step * 1e-3),
             "gpu_launches": args.steps * s.launches_per_step(kind)}
     print(json.dumps(line), flush=True)
     if dist:
@@ -397,10 +409,12 @@ def measure_e2e(s, w, kind, args, stream):
     ins = [s.tokens, s.prefix_len, s.q, s.k_new, s.v_new, s.logits]
     if kind in ("mss", "both"):
         ins += [s.ssm, s.uniforms]
+    if kind == "naive":
+        ins += [s.uniforms]
     if w.tree_mode == "chains":
         ins += [s.chains, s.root_token]
     host_in = [pinned(t) for t in ins]
-    outs = [s.mss_tokens, s.mss_count] if kind == "mss" else [s.out_tokens, s.out_count]
+    outs = [s.mss_tokens, s.mss_count] if kind in ("mss", "naive") else [s.out_tokens, s.out_count]
     outs.append(s.new_prefix_len)
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
@@ -437,6 +451,8 @@ def main():
     ap.add_argument("--config", default="llama7b", choices=sorted(DESCR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify", default=None, choices=["greedy", "mss", "naive", "both"],
+                    help="verifier of the step (default: the workload's)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host instead of a CUDA graph")
     ap.add_argument("--scale-down", type=int, default=1,
                     help="divide the batch (and the long prefix) by N: a smaller case of the same kernels, for profiling")

@@ -15,6 +15,7 @@
  *                    in one kernel, topology-aware mask built in registers
  *   verify_greedy    VerifyGreedy (Algorithm 2)
  *   verify_mss       VerifyStochastic: multi-step speculative sampling (Algorithm 2)
+ *   verify_naive     naive sampling, the comparison verifier of sec. 4.3 / 6.6
  *   kv_commit        keep only the accepted path's K/V (sec. 4.2, last paragraph)
  *
  * Conventions shared by every call
@@ -205,6 +206,20 @@ ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
                      const float *ssm_probs, const int32_t *q_row, int NQ, const float *uniforms,
                      float temperature, const ts_tree *t, int V, uint32_t *status,
                      cudaStream_t stream);
+
+/*
+ * verify_naive -- naive sampling (SpecInfer sec. 4.3, the verifier that
+ * multi-step speculative sampling is compared with in sec. 6.6 / Table 3):
+ * at the visited node u draw x from p = softmax(logits_u / T) by inverse CDF
+ * with uniforms[b][1][u] (the first x, by id, with C(x) > u * sum p); if a
+ * child of u (in input order) has token x, accept it and continue there,
+ * else append x and stop. Arguments as verify_mss without the drafter rows;
+ * uniforms[b][0][*] are not read. Same outputs, status bits and
+ * floating-point rules as verify_mss.
+ */
+ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *target_logits,
+                       const int32_t *p_row, int NP, const float *uniforms, float temperature,
+                       const ts_tree *t, int V, uint32_t *status, cudaStream_t stream);
 
 /*
  * kv_commit -- keep the accepted path's K/V (SpecInfer sec. 4.2: only the

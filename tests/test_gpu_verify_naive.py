@@ -1,0 +1,159 @@
+"""verify_naive (naive sampling, SpecInfer sec. 4.3 / 6.6) on the GPU against the
+oracle's or_verify_naive: tokens bit-exact and counts equal up to the first
+draw whose uniform lies within 1e-6 (relative) of a cumulative-sum boundary --
+those draws are decided in different precisions on the two sides and the
+requests that contain one are counted, not compared past that draw."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_speculative_verification_gb300 import api
+from tree_speculative_verification_gb300.step import to_device
+
+from _helpers import oracle_tree, workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _children(par, u, n):
+    return [v for v in range(n) if par[v] == u]
+
+
+def _low_margin_pos(logits_nodes, par, tok, n, uni_s, T, out_tokens, count):
+    """Position of the first low-margin draw along the oracle's path (count if none)."""
+    u = int(np.nonzero(par[:n] == -1)[0][0])
+    for i in range(int(count)):
+        z = logits_nodes[u].astype(np.float64) / T
+        p = np.exp(z - z.max())
+        c = np.cumsum(p)
+        tgt = float(uni_s[u]) * c[-1]
+        x = int(out_tokens[i])
+        lo = c[x - 1] if x > 0 else 0.0
+        if min(abs(c[x] - tgt), abs(tgt - lo)) < 1e-6 * c[-1]:
+            return i
+        nxt = [v for v in _children(par, u, n) if tok[v] == x]
+        if not nxt:
+            break
+        u = nxt[0]
+    return int(count)
+
+
+def _run(logits_nodes, par, tok, n_nodes, uni, T, p_row=None, logits_rows=None):
+    B, n_max = par.shape
+    t = api.Tree(B, n_max)
+    d = lambda a: to_device(a, "cuda")
+    api.tree_build(t, d(tok), d(par), d(n_nodes))
+    ot = torch.full((B, n_max + 1), -1, dtype=torch.int32, device="cuda")
+    op = torch.full((B, n_max + 1), -1, dtype=torch.int32, device="cuda")
+    oc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = logits_nodes if logits_rows is None else logits_rows
+    api.verify_naive(ot, op, oc, d(rows), d(uni), T, t, p_row=None if p_row is None else d(p_row), status=st)
+    torch.cuda.synchronize()
+    return ot.cpu().numpy(), op.cpu().numpy(), oc.cpu().numpy(), int(st.item())
+
+
+def _compare(logits_nodes, par, tok, n_nodes, uni, T, got, max_excluded):
+    ot, op, oc, _ = got
+    ref = oracle.verify_naive(logits_nodes, par, tok, n_nodes, uni, T)
+    excluded = 0
+    for b in range(par.shape[0]):
+        n = int(n_nodes[b])
+        rc = int(ref["count"][b])
+        lm = _low_margin_pos(logits_nodes[b], par[b], tok[b], n, uni[b, 1], T, ref["tokens"][b], rc)
+        k = min(lm, rc)
+        assert ot[b, :k].tolist() == ref["tokens"][b, :k].tolist(), b
+        if lm >= rc:
+            assert oc[b] == rc, b
+        else:
+            excluded += 1
+        # the path: op[0] is the root, op[i + 1] a child of op[i] whose token is ot[i]
+        assert par[b, op[b, 0]] == -1
+        for i in range(int(oc[b]) - 1):
+            assert par[b, op[b, i + 1]] == op[b, i] and tok[b, op[b, i + 1]] == ot[b, i]
+    assert excluded <= max_excluded, excluded
+    return ref
+
+
+@pytest.mark.parametrize("V", [8, 257, 1000, 32000])
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_naive_random_trees(V, T):
+    """Random topologies; each child's token drawn from the target at its parent,
+    so that draws often match a child and walks go several levels deep; V = 257
+    exercises the scalar path."""
+    rng = np.random.default_rng(V + int(100 * T))
+    B, n = 64, 12
+    par = np.full((B, n), -1, np.int32)
+    for b in range(B):
+        for v in range(1, n):
+            par[b, v] = rng.integers(0, v)
+    logits = (rng.standard_normal((B, n, V)) * 2.0).astype(np.float32)
+    # a peaked target (one token lifted by 8 per row), as a language model's is
+    logits[np.arange(B)[:, None], np.arange(n)[None, :], rng.integers(0, V, (B, n))] += 8.0
+    tok = np.zeros((B, n), np.int32)
+    for b in range(B):
+        for v in range(1, n):
+            z = logits[b, par[b, v]].astype(np.float64) / T
+            p = np.exp(z - z.max())
+            tok[b, v] = min(int(np.searchsorted(np.cumsum(p), rng.random() * p.sum(), side="right")), V - 1)
+    uni = rng.random((B, 2, n)).astype(np.float32)
+    nn = np.full(B, n, np.int32)
+    # with 32000 entries the drawn token itself often holds under 1e-6 of the mass,
+    # which puts both of its cumulative-sum boundaries inside the margin
+    ref = _compare(logits, par, tok, nn, uni, T, _run(logits, par, tok, nn, uni, T),
+                   max_excluded=3 if V < 32000 else B // 5)
+    assert ref["count"].max() >= 2   # some walks accept at least one child
+
+
+def test_naive_merge_workload_with_row_map():
+    """The merged-chains layer at full size: node rows come through p_row."""
+    w = workload("merge", attention=False)
+    parent, tokens, n_nodes, p_row, _ = oracle_tree(w)
+    logits_nodes = np.stack([w.logits[b][p_row[b]] for b in range(w.B)])   # the oracle reads one row per node
+    got = _run(logits_nodes, parent, tokens, n_nodes, w.uniforms, w.temperature, p_row=p_row, logits_rows=w.logits)
+    _compare(logits_nodes, parent, tokens, n_nodes, w.uniforms, w.temperature, got, max_excluded=1)
+
+
+def test_naive_nonfinite_row_empties_the_request():
+    rng = np.random.default_rng(5)
+    B, n, V = 3, 4, 64
+    par = np.tile(np.array([-1, 0, 0, 1], np.int32), (B, 1))
+    logits = rng.standard_normal((B, n, V)).astype(np.float32)
+    logits[1, 0, 7] = np.inf                 # request 1's root row: the walk reads it first
+    tok = rng.integers(0, V, (B, n)).astype(np.int32)
+    uni = rng.random((B, 2, n)).astype(np.float32)
+    ot, op, oc, st = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
+    assert oc[1] == 0 and oc[0] >= 1 and oc[2] >= 1
+    assert st & api.STATUS_NONFINITE
+
+
+def test_mss_accepts_at_least_as_many_tokens_as_naive():
+    """SpecInfer Thm 4.3 on the GPU: over many requests with a drafter close to
+    the target, multi-step speculative sampling accepts no fewer tokens per
+    step on average than naive sampling (same trees, same uniforms)."""
+    rng = np.random.default_rng(11)
+    B, n, V = 256, 7, 512
+    par = np.tile(np.array([-1, 0, 0, 1, 1, 2, 2], np.int32), (B, 1))
+    logits = (rng.standard_normal((B, n, V)) * 2.0).astype(np.float32)
+    z = logits + (0.5 * rng.standard_normal((B, n, V))).astype(np.float32)
+    q = np.exp(z - z.max(-1, keepdims=True)); q /= q.sum(-1, keepdims=True); q = q.astype(np.float32)
+    tok = np.zeros((B, n), np.int32)
+    for b in range(B):
+        for v in range(1, n):
+            cdf = np.cumsum(q[b, par[b, v]].astype(np.float64))
+            tok[b, v] = min(int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right")), V - 1)
+    uni = rng.random((B, 2, n)).astype(np.float32)
+    _, _, naive_counts, _ = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
+    t = api.Tree(B, n)
+    d = lambda a: to_device(a, "cuda")
+    api.tree_build(t, d(tok), d(par), d(np.full(B, n, np.int32)))
+    ot = torch.full((B, n + 1), -1, dtype=torch.int32, device="cuda")
+    op = torch.full((B, n + 1), -1, dtype=torch.int32, device="cuda")
+    oc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    q_row = np.where(par >= 0, par, 0).astype(np.int32)
+    api.verify_mss(ot, op, oc, d(logits), d(q), d(q_row), d(uni), 1.0, t)
+    torch.cuda.synchronize()
+    mss_mean, naive_mean = float(oc.float().mean()), float(naive_counts.mean())
+    print(f"accepted tokens per step: MSS {mss_mean:.3f}, naive {naive_mean:.3f}")
+    assert mss_mean >= naive_mean

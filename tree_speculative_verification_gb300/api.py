@@ -25,7 +25,7 @@ MAX_NODES = 256
 #: every entry point of the C ABI (include/treespec.h)
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
-           "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel")
+           "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -62,6 +62,7 @@ def load_library(path: str | None = None):
         "tree_attention": [P, P, P, P, P, T, I, I, I, I, F, P, Z, P, P],
         "verify_greedy": [P, P, P, P, P, T, I, P, Z, P, P],
         "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
+        "verify_naive": [P, P, P, P, P, I, P, F, T, I, P, P],
         "kv_commit": [P, P, P, P, P, P, T, I, I, I, I, P, P],
         "treespec_workspace_init": [P, Z, P],
         "tree_attention_noalloc": [P, P, P, P, P, T, I, I, I, I, F, P, P],
@@ -220,6 +221,15 @@ def verify_mss(out_tokens, out_path, out_count, target_logits, ssm_probs, q_row,
     _check(lib.verify_mss(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(target_logits),
                           _ptr(_i32(p_row, "p_row")), NP, _ptr(ssm_probs), _ptr(_i32(q_row, "q_row")), NQ,
                           _ptr(uniforms), float(temperature), tree.c, V, _ptr(status), _stream(stream)), "verify_mss")
+
+
+def verify_naive(out_tokens, out_path, out_count, target_logits, uniforms, temperature, tree: Tree, p_row=None,
+                 status=None, stream=None):
+    lib = load_library()
+    NP, V = target_logits.shape[1], target_logits.shape[2]
+    _check(lib.verify_naive(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(target_logits),
+                            _ptr(_i32(p_row, "p_row")), NP, _ptr(uniforms), float(temperature), tree.c, V,
+                            _ptr(status), _stream(stream)), "verify_naive")
 
 
 def kv_commit(k_cache, v_cache, prefix_len, new_prefix_len, out_path, out_count, tree: Tree, status=None,

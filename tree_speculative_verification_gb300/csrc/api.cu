@@ -211,6 +211,25 @@ ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
                        "verify_mss");
 }
 
+ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *target_logits,
+                       const int32_t *p_row, int NP, const float *uniforms, float temperature, const ts_tree *t,
+                       int V, uint32_t *status, cudaStream_t stream) {
+    ts_status st = check_tree(t, "verify_naive");
+    if (st) return st;
+    if (!out_tokens || !out_path || !out_count || !target_logits || !uniforms)
+        return fail(TS_ERR_INVALID_ARG, "verify_naive: NULL pointer");
+    if (V < 1) return fail(TS_ERR_INVALID_ARG, "verify_naive: V=%d must be >= 1", V);
+    if (!(temperature > 0.f)) return fail(TS_ERR_INVALID_ARG, "verify_naive: temperature must be > 0");
+    if (!p_row && NP < t->n_max)
+        return fail(TS_ERR_INVALID_ARG, "verify_naive: without p_row, NP=%d must be >= n_max=%d", NP, t->n_max);
+    if (NP < 1) return fail(TS_ERR_INVALID_ARG, "verify_naive: NP=%d must be >= 1", NP);
+    if (V % 4 == 0 && !aligned16(target_logits))
+        return fail(TS_ERR_INVALID_ARG, "verify_naive: target_logits must be 16-byte aligned");
+    return cuda_result(ts::launch_verify_naive(out_tokens, out_path, out_count, target_logits, p_row, NP, uniforms,
+                                               temperature, *t, V, status, stream),
+                       "verify_naive");
+}
+
 ts_status kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int32_t *new_prefix_len,
                     const int32_t *out_path, const int32_t *out_count, const ts_tree *t, int H, int d, int L_max,
                     ts_dtype dtype, uint32_t *status, cudaStream_t stream) {

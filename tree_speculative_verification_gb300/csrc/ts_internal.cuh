@@ -107,6 +107,10 @@ cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *o
                               const int32_t *q_row, int NQ, const float *uniforms, float temperature,
                               const ts_tree &t, int V, uint32_t *status, cudaStream_t s);
 
+cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+                                const float *logits, const int32_t *p_row, int NP, const float *uniforms,
+                                float temperature, const ts_tree &t, int V, uint32_t *status, cudaStream_t s);
+
 int num_sms();
 
 ts_status set_error(ts_status st, const char *fmt, ...);

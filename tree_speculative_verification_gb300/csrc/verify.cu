@@ -6,7 +6,7 @@
 // verify_greedy: node-parallel. Every (request, node, vocab segment) CTA
 //   streams its slice of the target logits once (argmax, lowest id on ties);
 //   the last CTA of a request merges the segments and walks the tree.
-// verify_mss: walk-first. One 1024-thread CTA per request follows Algorithm 2
+// verify_mss / verify_naive: walk-first. One 1024-thread CTA per request follows Algorithm 2
 //   and touches only the rows on the accepted path (the target row of each
 //   visited node, the drafter rows of its tested children); each step is a
 //   block-wide reduction over the vocabulary. Elementwise work is fp32; sums
@@ -309,8 +309,11 @@ __device__ int block_or(MssShared &sm, int x) {
 // One CTA per request, walking the tree as Algorithm 2 does. SMEM_R keeps the
 // residual row of the current node in shared memory (vocabularies up to ~53K
 // entries): the exps are taken once per visited node and a rejection is one
-// in-place pass over R and one drafter row.
-template <bool SMEM_R>
+// in-place pass over R and one drafter row. NAIVE: naive sampling instead
+// (SpecInfer sec. 4.3): at each visited node draw x from p by the same inverse
+// CDF, move to the first child whose token is x, else append x and stop; no
+// drafter rows are read.
+template <bool SMEM_R, bool NAIVE>
 __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
                                                         const float *logits, const int32_t *p_row, int NP,
                                                         const float *ssm, const int32_t *q_row, int NQ,
@@ -342,7 +345,9 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         const int pr = p_row ? p_row[(size_t)b * n_max + v] : v;
         sm.prow[i] = pr;
         if (pr < 0 || pr >= NP) bad_index = 1;
-        if (i > 0) {
+        if (i > 0 && NAIVE) {
+            if (sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
+        } else if (i > 0) {
             const int qr = q_row[(size_t)b * n_max + v];
             sm.qrow[i] = qr;
             if (qr < 0 || qr >= NQ || sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         // child, the final-sample uniform of u
         {
             const int du = sm.depth[u], se_u = sm.sub_end[u];
-            for (int i = u + 1 + tid; i < se_u; i += kMssThreads)
+            for (int i = u + 1 + tid; !NAIVE && i < se_u; i += kMssThreads)
                 if (sm.depth[i] == du + 1) {
                     sm.cq[i] = __ldg(ssm + ((size_t)b * NQ + sm.qrow[i]) * V + sm.tok[i]);
                     sm.cu[i] = __ldg(u_acc + sm.perm[i]);
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         // children in input order: u+1, sub_end[u+1], ... below sub_end[u]
         int nrej = 0;
         int accepted = -1;
-        for (int c = u + 1; c < sm.sub_end[u]; c = sm.sub_end[c]) {
+        for (int c = u + 1; !NAIVE && c < sm.sub_end[u]; c = sm.sub_end[c]) {
             const float *qc = ssm + ((size_t)b * NQ + sm.qrow[c]) * V;
             const int x = sm.tok[c];
             const Resid rr{row, invT, m, sm.rej_q, sm.rej_S, nrej, Rs};
@@ -630,10 +635,27 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                 }
             }
             if (chosen < 0) chosen = last_pos >= 0 ? last_pos : 0;
-            if (lane == 0) ot[cnt] = chosen;
+            if (lane == 0) {
+                ot[cnt] = chosen;
+                sm.token = chosen;
+            }
         }
         ++cnt;
-        break;
+        if (!NAIVE) break;
+        // naive sampling: continue at the first child holding the drawn token
+        __syncthreads();
+        if (tid == 0) {
+            int next = -1;
+            for (int c = u + 1; c < sm.sub_end[u]; c = sm.sub_end[c])
+                if (sm.tok[c] == sm.token) { next = c; break; }
+            sm.pick = next;
+            if (next >= 0) op[cnt] = sm.perm[next];
+        }
+        __syncthreads();
+        const int next = sm.pick;
+        __syncthreads();   // the next node's pass 1 overwrites R and pick
+        if (next < 0) break;
+        u = next;
     }
     if (tid == 0) {
         if (nonfinite) {
@@ -676,22 +698,39 @@ cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t
                   V, seg, vec4, counters, parts, status);
 }
 
-cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
-                              const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
-                              const float *uniforms, float temperature, const ts_tree &t, int V,
-                              uint32_t *status, cudaStream_t s) {
+template <bool NAIVE>
+cudaError_t launch_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
+                        const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
+                        const float *uniforms, float temperature, const ts_tree &t, int V, uint32_t *status,
+                        cudaStream_t s) {
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const size_t with_row = kMssHeader + (size_t)((V + 3) & ~3) * sizeof(float);
     if (with_row <= (size_t)optin) {
-        cudaError_t e = cudaFuncSetAttribute(k_mss<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_row);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_mss<true, NAIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_row);
         if (e != cudaSuccess) return e;
-        return launch(k_mss<true>, dim3(t.B), dim3(kMssThreads), with_row, s, out_tokens, out_path, out_count, logits,
-                      p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+        return launch(k_mss<true, NAIVE>, dim3(t.B), dim3(kMssThreads), with_row, s, out_tokens, out_path, out_count,
+                      logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
     }
-    return launch(k_mss<false>, dim3(t.B), dim3(kMssThreads), (size_t)kMssHeader, s, out_tokens, out_path, out_count,
-                  logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+    return launch(k_mss<false, NAIVE>, dim3(t.B), dim3(kMssThreads), (size_t)kMssHeader, s, out_tokens, out_path,
+                  out_count, logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+}
+
+cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
+                              const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
+                              const float *uniforms, float temperature, const ts_tree &t, int V,
+                              uint32_t *status, cudaStream_t s) {
+    return launch_walk<false>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row, NQ, uniforms,
+                              temperature, t, V, status, s);
+}
+
+cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
+                                const int32_t *p_row, int NP, const float *uniforms, float temperature,
+                                const ts_tree &t, int V, uint32_t *status, cudaStream_t s) {
+    return launch_walk<true>(out_tokens, out_path, out_count, logits, p_row, NP, nullptr, nullptr, 1, uniforms,
+                             temperature, t, V, status, s);
 }
 
 }  // namespace ts

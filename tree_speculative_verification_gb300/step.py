@@ -3,7 +3,7 @@
 DeviceStep holds a workload's tensors on the device (KV cache, Q / new K/V,
 logits, drafter probabilities, uniforms) and the output buffers, and runs the
 hot path: tree_build -> kv_append -> tree_attention -> verify (greedy and/or
-MSS) -> kv_commit. kv_commit writes the new prefix lengths into a separate
+MSS, or naive sampling) -> kv_commit. kv_commit writes the new prefix lengths into a separate
 array, so repeating a step on the same inputs is idempotent.
 """
 from __future__ import annotations
@@ -96,10 +96,14 @@ class DeviceStep:
             api.verify_mss(self.mss_tokens, self.mss_path, self.mss_count, self.logits, self.ssm, self.q_row,
                            self.uniforms, self.w.temperature, self.tree, p_row=self.p_row, status=self.status,
                            stream=stream)
+        if kind == "naive":
+            api.verify_naive(self.mss_tokens, self.mss_path, self.mss_count, self.logits, self.uniforms,
+                             self.w.temperature, self.tree, p_row=self.p_row, status=self.status, stream=stream)
 
     def commit(self, kind: str | None = None, stream=None):
         kind = kind or self.w.verify
-        path, count = (self.mss_path, self.mss_count) if kind in ("mss", "both") else (self.out_path, self.out_count)
+        path, count = ((self.mss_path, self.mss_count) if kind in ("mss", "both", "naive")
+                       else (self.out_path, self.out_count))
         api.kv_commit(self.k_cache, self.v_cache, self.prefix_len, self.new_prefix_len, path, count, self.tree,
                       self.status, stream)
 
@@ -111,6 +115,12 @@ class DeviceStep:
         self.verify(kind, stream)
         if self.attention:
             self.commit(kind, stream)
+
+    def accepted(self, kind: str | None = None) -> int:
+        """Tokens the last verification produced, over all requests."""
+        kind = kind or self.w.verify
+        count = self.mss_count if kind in ("mss", "both", "naive") else self.out_count
+        return int(count.sum().item())
 
     def launches_per_step(self, kind: str | None = None) -> int:
         kind = kind or self.w.verify
