@@ -348,6 +348,38 @@ def run_ours(args):
         sampler.stop()
     t_att = evs["attend"][0].elapsed_time(evs["attend"][1]) / K
     t_ver = evs["verify"][0].elapsed_time(evs["verify"][1]) / K
+    seq_line = None
+    if args.sequence_baseline and rank == 0:
+        # SpecInfer Fig. 4 (left) / Fig. 11: one sequence and one prefix copy per
+        # root-to-leaf path, the same attention call on the chains
+        seq_w, path_nodes = workloads.sequence_batch(w)
+        seq_w.n_nodes_dev = seq_w.n_nodes
+        sq = DeviceStep(seq_w, device)
+        sq.build()
+        sq.append()
+        torch.cuda.synchronize()
+        ge = _events(2, True)
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device)
+        cs.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+            cur = torch.cuda.current_stream(device)
+            ge[0].record(cur)
+            for _ in range(K):
+                sq.attend()
+            ge[1].record(cur)
+        stream.wait_stream(cs)
+        g.replay()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        t_seq = ge[0].elapsed_time(ge[1]) / K
+        seq_line = {"paths": int(seq_w.B), "path_nodes": int(seq_w.n_nodes.sum()), "attention_ms": t_seq,
+                    "algorithmic_bytes_per_launch": attention_bytes(seq_w),
+                    "tree_speedup": t_seq / t_att,
+                    "kernel": api.attention_kernel(seq_w.B, seq_w.H, seq_w.n_max, seq_w.d, seq_w.L_max,
+                                                   api.TS_BF16 if seq_w.dtype == "bf16" else api.TS_F32)}
+        del sq, g
     if dist:
         tt = torch.tensor([ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -392,6 +424,7 @@ def run_ours(args):
             "attention_ms": t_att, "verify_ms": t_ver,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "accepted_tokens_per_step": accepted_per_step,
+            **({"sequence_baseline": seq_line} if seq_line else {}),
             "accepted_tokens_per_s": ws * accepted_per_step / (ms_per_step * 1e-3),
             "gpu_launches": args.steps * s.launches_per_step(kind)}
     print(json.dumps(line), flush=True)
@@ -451,6 +484,8 @@ def main():
     ap.add_argument("--config", default="llama7b", choices=sorted(DESCR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sequence-baseline", action="store_true",
+                    help="also time attention as one sequence per root-to-leaf path (SpecInfer Fig. 4 left)")
     ap.add_argument("--verify", default=None, choices=["greedy", "mss", "naive", "both"],
                     help="verifier of the step (default: the workload's)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host instead of a CUDA graph")

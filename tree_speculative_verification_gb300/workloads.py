@@ -331,3 +331,50 @@ def _make_merge(rng, attention, sd):
     if attention:
         w.q, w.k_new, w.v_new, w.k_cache, w.v_cache = _qkv(rng, B, n_max, H, d, L_max, prefix_len, "bf16")
     return w
+
+
+def sequence_batch(w: Workload) -> tuple[Workload, np.ndarray]:
+    """The sequence-based decoding baseline of SpecInfer Fig. 4 (left) / Fig. 11
+    as inputs: every root-to-leaf path of every request becomes a request of its
+    own -- a chain over the path's nodes, with its own copy of the prefix K/V.
+    Returns the chain workload (attention inputs only) and path_nodes
+    [paths][len] = (request, input node) of each chain position (-1 padding).
+    Needs a workload built with attention and a parent array."""
+    assert w.q is not None and w.parent is not None, "sequence_batch needs attention inputs and a parent array"
+    paths = []
+    for b in range(w.B):
+        n = int(w.n_nodes[b])
+        par = w.parent[b, :n]
+        leaves = [v for v in range(n) if not np.any(par == v)]
+        for leaf in leaves:
+            p, u = [], leaf
+            while u != -1:
+                p.append(u)
+                u = int(par[u])
+            paths.append((b, p[::-1]))
+    S = len(paths)
+    n_max = max(len(p) for _, p in paths)
+    P = np.array([w.prefix_len[b] for b, _ in paths], np.int32)
+    L_max = _round_up(int(P.max()) + n_max, 64)
+    path_nodes = np.full((S, n_max, 2), -1, np.int32)
+    parent = np.full((S, n_max), -1, np.int32)
+    n_nodes = np.zeros(S, np.int32)
+    q = np.zeros((S, n_max) + w.q.shape[2:], w.q.dtype)
+    k_new, v_new = np.zeros_like(q), np.zeros_like(q)
+    k_cache = np.zeros((S, w.H, L_max, w.d), w.k_cache.dtype)
+    v_cache = np.zeros_like(k_cache)
+    for s, (b, p) in enumerate(paths):
+        m = len(p)
+        n_nodes[s] = m
+        parent[s, 1:m] = np.arange(m - 1)
+        path_nodes[s, :m, 0] = b
+        path_nodes[s, :m, 1] = p
+        q[s, :m], k_new[s, :m], v_new[s, :m] = w.q[b, p], w.k_new[b, p], w.v_new[b, p]
+        k_cache[s, :, :P[s]] = w.k_cache[b, :, :P[s]]
+        v_cache[s, :, :P[s]] = w.v_cache[b, :, :P[s]]
+    seq = Workload(name=w.name + "-sequences", B=S, H=w.H, d=w.d, dtype=w.dtype, V=1, n_max=n_max, L_max=L_max,
+                   verify="greedy", temperature=1.0, prefix_len=P, tree_mode="parent", n_nodes=n_nodes,
+                   parent=parent, tokens=np.zeros((S, n_max), np.int32),
+                   logits=np.zeros((S, n_max, 1), np.float32), uniforms=np.zeros((S, 2, n_max), np.float32))
+    seq.q, seq.k_new, seq.v_new, seq.k_cache, seq.v_cache = q, k_new, v_new, k_cache, v_cache
+    return seq, path_nodes
