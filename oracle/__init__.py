@@ -89,6 +89,23 @@ def widths_parent(widths, n_cap: int = 4096) -> np.ndarray:
     return par[:n].copy()
 
 
+def topk_expand(widths, root_token, ssm, n_max: int | None = None):
+    """Tokens of the expansion tree <k1..km> drafted by top-k (sec. 3, Fig. 3):
+    node u's children are the k most probable tokens of ssm[b][u], ties to the
+    lower id. Returns (tokens [B][n_max], status bits)."""
+    lib = _load()
+    w = _i32(widths)
+    q = _f32(ssm)
+    B, NQ, V = q.shape
+    n = len(widths_parent(widths))
+    n_max = n if n_max is None else n_max
+    rt = _i32(root_token)
+    tok = np.full((B, n_max), -1, np.int32)
+    st = lib.or_topk_expand(C.c_int(B), C.c_int(n_max), C.c_int(NQ), C.c_int(V), C.c_int(len(w)), _p(w), _p(rt),
+                            _p(q), _p(tok))
+    return tok, int(st)
+
+
 def merge_chains(chains, root_token: int, n_cap: int | None = None):
     """Trie merge of C chains of equal length (Def. 3.2).
     Returns (parent, tokens, src) in creation order; src = chain*len + pos."""

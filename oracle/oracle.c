@@ -194,6 +194,54 @@ int or_widths_parent(int m, const int32_t *widths, int n_cap, int32_t *parent) {
     return n;
 }
 
+/* Top-k expansion from the drafter ([SI] sec. 3, Fig. 3: the SSM expands each
+ * node of depth i-1 into its k_i most likely next tokens). For the expansion
+ * tree <k1..km> in level order (or_widths_parent), node u's children take, in
+ * order, the k most probable tokens of drafter row u (ssm [B][NQ][V]), ties to
+ * the lower token id: sort every token of the row by (probability desc, id
+ * asc) and take the first k. tokens[b][0] = root_token[b]. A row with a
+ * non-finite entry gives its children token -1 and sets OR_NONFINITE.
+ * Returns the status bits. */
+static const float *g_row;
+static int by_prob_then_id(const void *a, const void *b) {
+    int x = *(const int *)a, y = *(const int *)b;
+    double px = g_row[x], py = g_row[y];
+    if (px > py) return -1;
+    if (px < py) return 1;
+    return (x > y) - (x < y);
+}
+
+int or_topk_expand(int B, int n_max, int NQ, int V, int m, const int32_t *widths, const int32_t *root_token,
+                   const float *ssm, int32_t *tokens) {
+    int32_t *par = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_max);
+    int *ids = (int *)malloc(sizeof(int) * (size_t)V);
+    int all = 0;
+    int n = or_widths_parent(m, widths, n_max, par);
+    if (n < 0) { free(par); free(ids); return OR_BAD_ARG; }
+    for (int b = 0; b < B; ++b) {
+        int32_t *tok = tokens + (size_t)b * n_max;
+        for (int v = 0; v < n_max; ++v) tok[v] = -1;
+        tok[0] = root_token[b];
+        for (int u = 0; u < n; ++u) {
+            int first = -1, k = 0;
+            for (int v = 1; v < n; ++v)
+                if (par[v] == u) { if (first < 0) first = v; ++k; }
+            if (k == 0) continue;
+            if (u >= NQ) { all |= OR_BAD_ARG; continue; }
+            const float *row = ssm + ((size_t)b * NQ + u) * V;
+            int bad = 0;
+            for (int x = 0; x < V; ++x) { ids[x] = x; if (!isfinite(row[x])) bad = 1; }
+            if (bad) { all |= OR_NONFINITE; continue; }
+            g_row = row;
+            qsort(ids, (size_t)V, sizeof(int), by_prob_then_id);
+            for (int c = 0; c < k && c < V; ++c) tok[first + c] = ids[c];
+        }
+    }
+    free(par);
+    free(ids);
+    return all;
+}
+
 /* Merge of chains ([SI] Def. 3.2): every node stands for one distinct token
  * sequence; insert the chains one after another into a trie rooted at the
  * committed token. New nodes are numbered in creation order. src[v] gives the
