@@ -9,6 +9,9 @@
  *   tree_build       linearise a token tree in depth-first order (sec. 4.2,
  *                    Fig. 4) from a parent array, an expansion configuration
  *                    <k1..km> (sec. 3, Fig. 3) or merged drafter chains (Def. 3.2)
+ *   tree_expand_topk draft an expansion tree <k1..km> from drafter distributions
+ *                    (sec. 3, Fig. 3: each node's children are its k most likely
+ *                    next tokens)
  *   kv_append        write the tree nodes' K/V after the verified prefix of one
  *                    shared KV cache, in depth-first order (sec. 4.2)
  *   tree_attention   TreeAttention(u) = Attention(S_u) for every node (Def. 4.1)
@@ -132,6 +135,25 @@ ts_status tree_build(const ts_tree *t, const int32_t *tokens, const int32_t *par
 ts_status tree_build_chains(const ts_tree *t, const int32_t *root_token, const int32_t *chains,
                             int C, int len, int32_t *tokens_out, int32_t *p_row, int32_t *q_row,
                             const int32_t *prefix_len, uint32_t *status, cudaStream_t stream);
+
+/*
+ * tree_expand_topk -- the drafter's top-k expansion (SpecInfer sec. 3, Fig. 3:
+ * every node of depth i-1 gets the k_i most likely next tokens as children).
+ * For the expansion tree <widths[0..m-1]> numbered level by level (as
+ * tree_build's widths mode numbers it), the children of internal node u take,
+ * best first, the widths[depth(u)] most probable tokens of ssm_probs[b][u],
+ * ties to the lower token id; tokens[b][0] = root_token[b].
+ *   tokens      [B][n_max]  out: the tree's tokens in level order (entries past
+ *                           the tree's size are not written)
+ *   root_token  [B]
+ *   ssm_probs   [B][NQ][V]  fp32, row u = drafter distribution after node u;
+ *                           NQ >= the number of internal nodes
+ * A non-finite value in a row gives that node's children token -1 and sets
+ * TS_STATUS_NONFINITE. The result feeds tree_build(..., widths, m, ...).
+ */
+ts_status tree_expand_topk(int32_t *tokens, const int32_t *root_token, const float *ssm_probs, int NQ,
+                           int B, int n_max, const int32_t *widths, int m, int V, uint32_t *status,
+                           cudaStream_t stream);
 
 /*
  * kv_append -- place the pass's fresh K/V in the shared cache in depth-first

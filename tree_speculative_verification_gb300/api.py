@@ -25,7 +25,8 @@ MAX_NODES = 256
 #: every entry point of the C ABI (include/treespec.h)
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
-           "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive")
+           "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive",
+           "tree_expand_topk")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -63,6 +64,7 @@ def load_library(path: str | None = None):
         "verify_greedy": [P, P, P, P, P, T, I, P, Z, P, P],
         "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
         "verify_naive": [P, P, P, P, P, I, P, F, T, I, P, P],
+        "tree_expand_topk": [P, P, P, I, I, I, P, I, I, P, P],
         "kv_commit": [P, P, P, P, P, P, T, I, I, I, I, P, P],
         "treespec_workspace_init": [P, Z, P],
         "tree_attention_noalloc": [P, P, P, P, P, T, I, I, I, I, F, P, P],
@@ -158,6 +160,17 @@ def tree_build_chains(tree: Tree, root_token, chains, tokens_out=None, p_row=Non
                                  _ptr(_i32(tokens_out, "tokens_out")), _ptr(_i32(p_row, "p_row")),
                                  _ptr(_i32(q_row, "q_row")), _ptr(_i32(prefix_len, "prefix_len")), _ptr(status),
                                  _stream(stream)), "tree_build_chains")
+
+
+def tree_expand_topk(tokens, root_token, ssm_probs, widths, status=None, stream=None):
+    """Draft the expansion tree <widths> from drafter rows into tokens [B][n_max]."""
+    lib = load_library()
+    B, n_max = tokens.shape
+    NQ, V = ssm_probs.shape[1], ssm_probs.shape[2]
+    m = len(widths)
+    w_arr = (C.c_int32 * max(1, m))(*[int(k) for k in widths])
+    _check(lib.tree_expand_topk(_ptr(_i32(tokens, "tokens")), _ptr(_i32(root_token, "root_token")), _ptr(ssm_probs),
+                                NQ, B, n_max, w_arr, m, V, _ptr(status), _stream(stream)), "tree_expand_topk")
 
 
 def kv_append(k_cache, v_cache, k_new, v_new, prefix_len, tree: Tree, status=None, stream=None):

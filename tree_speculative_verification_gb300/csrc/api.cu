@@ -82,6 +82,38 @@ const char *treespec_last_error(void) { return g_err; }
 
 const char *treespec_version(void) { return "treespec 0.1 (sm_103a)"; }
 
+// Expansion configuration <k1..km> -> level layout (shared by tree_build and
+// tree_expand_topk); false with a message on bad widths.
+static bool widths_param(const int32_t *widths, int m, int n_max, ts::WidthsParam &w, const char *who) {
+    if (m < 0 || m > 16) {
+        ts::set_error(TS_ERR_INVALID_ARG, "%s: %d expansion levels (at most 16)", who, m);
+        return false;
+    }
+    w = ts::WidthsParam{};
+    w.m = m;
+    w.level_start[0] = 0;
+    w.level_start[1] = 1;
+    long long level_n = 1, n = 1;
+    for (int l = 0; l < m; ++l) {
+        if (widths[l] < 1) {
+            ts::set_error(TS_ERR_INVALID_ARG, "%s: widths[%d]=%d must be >= 1", who, l, widths[l]);
+            return false;
+        }
+        w.width[l] = widths[l];
+        level_n *= widths[l];
+        n += level_n;
+        if (n > n_max) {
+            ts::set_error(TS_ERR_INVALID_ARG, "%s: expansion tree has more than n_max=%d nodes", who, n_max);
+            return false;
+        }
+        w.level_start[l + 2] = (int)n;
+    }
+    w.n = (int)n;
+    w.sub[m] = 1;
+    for (int l = m - 1; l >= 0; --l) w.sub[l] = 1 + w.width[l] * w.sub[l + 1];
+    return true;
+}
+
 ts_status tree_build(const ts_tree *t, const int32_t *tokens, const int32_t *parent, const int32_t *n_nodes,
                      const int32_t *widths, int m, const int32_t *prefix_len, uint32_t *status,
                      cudaStream_t stream) {
@@ -89,29 +121,30 @@ ts_status tree_build(const ts_tree *t, const int32_t *tokens, const int32_t *par
     if (st) return st;
     if (!tokens) return fail(TS_ERR_INVALID_ARG, "tree_build: tokens is NULL");
     if (widths) {
-        if (m < 0 || m > 16) return fail(TS_ERR_INVALID_ARG, "tree_build: %d expansion levels (at most 16)", m);
-        ts::WidthsParam w{};
-        w.m = m;
-        w.level_start[0] = 0;
-        w.level_start[1] = 1;
-        long long level_n = 1, n = 1;
-        for (int l = 0; l < m; ++l) {
-            if (widths[l] < 1) return fail(TS_ERR_INVALID_ARG, "tree_build: widths[%d]=%d must be >= 1", l, widths[l]);
-            w.width[l] = widths[l];
-            level_n *= widths[l];
-            n += level_n;
-            if (n > t->n_max)
-                return fail(TS_ERR_INVALID_ARG, "tree_build: expansion tree has more than n_max=%d nodes", t->n_max);
-            w.level_start[l + 2] = (int)n;
-        }
-        w.n = (int)n;
-        w.sub[m] = 1;
-        for (int l = m - 1; l >= 0; --l) w.sub[l] = 1 + w.width[l] * w.sub[l + 1];
+        ts::WidthsParam w;
+        if (!widths_param(widths, m, t->n_max, w, "tree_build")) return TS_ERR_INVALID_ARG;
         return cuda_result(ts::launch_tree_build_widths(*t, tokens, w, prefix_len, status, stream), "tree_build");
     }
     if (!parent || !n_nodes) return fail(TS_ERR_INVALID_ARG, "tree_build: parent mode needs parent and n_nodes");
     return cuda_result(ts::launch_tree_build_parent(*t, tokens, parent, n_nodes, prefix_len, status, stream),
                        "tree_build");
+}
+
+ts_status tree_expand_topk(int32_t *tokens, const int32_t *root_token, const float *ssm_probs, int NQ, int B,
+                           int n_max, const int32_t *widths, int m, int V, uint32_t *status, cudaStream_t stream) {
+    if (!tokens || !root_token || !ssm_probs || !widths) return fail(TS_ERR_INVALID_ARG, "tree_expand_topk: NULL pointer");
+    if (B < 1 || n_max < 1 || n_max > TS_MAX_NODES)
+        return fail(TS_ERR_INVALID_ARG, "tree_expand_topk: B=%d, n_max=%d (1..%d)", B, n_max, TS_MAX_NODES);
+    if (V < 1) return fail(TS_ERR_INVALID_ARG, "tree_expand_topk: V=%d must be >= 1", V);
+    ts::WidthsParam w;
+    if (!widths_param(widths, m, n_max, w, "tree_expand_topk")) return TS_ERR_INVALID_ARG;
+    const int n_internal = w.level_start[m];   // every node above the last level has children
+    if (NQ < n_internal)
+        return fail(TS_ERR_INVALID_ARG, "tree_expand_topk: NQ=%d drafter rows, %d internal nodes", NQ, n_internal);
+    // one CTA per internal node (one for the root alone when m = 0: it writes the root token)
+    return cuda_result(ts::launch_expand_topk(tokens, root_token, ssm_probs, NQ, B, n_max, w,
+                                              n_internal > 0 ? n_internal : 1, V, status, stream),
+                       "tree_expand_topk");
 }
 
 ts_status tree_build_chains(const ts_tree *t, const int32_t *root_token, const int32_t *chains, int C, int len,

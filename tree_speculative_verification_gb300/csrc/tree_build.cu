@@ -10,6 +10,9 @@
 // The DFS index of v is the sum, over the nodes on its root path, of
 // 1 + (sizes of the earlier siblings), which needs only subtree sizes and
 // sibling order -- no sequential traversal.
+#include <climits>
+#include <math.h>
+
 #include "ts_internal.cuh"
 
 namespace ts {
@@ -271,6 +274,89 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_chains(ts_tree t, const int
     linearize(t, b, n, sm, P, status);
 }
 
+// Top-k expansion (sec. 3, Fig. 3: the SSM expands each node of depth i-1
+// into its k_i most likely next tokens). One CTA per (internal node u,
+// request): u's children, consecutive in level order, take the k best tokens
+// of drafter row u in the order (probability desc, id asc). Pass r keeps the
+// best entry that ranks strictly below the pass r-1 pick in that order, so k
+// passes over the row need no list of picked tokens.
+constexpr int kExpandThreads = 256;
+
+__device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(kExpandThreads) k_expand_topk(int32_t *tokens, const int32_t *root_token,
+                                                                const float *ssm, int NQ, WidthsParam w, int V,
+                                                                int n_max, bool vec4, uint32_t *status) {
+    const int u = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (u == 0 && tid == 0) tokens[(size_t)b * n_max] = root_token[b];
+    int l = 0;
+    while (l < w.m && u >= w.level_start[l + 1]) ++l;
+    if (l >= w.m) return;   // a leaf (only for m = 0: the root alone)
+    const int k = w.width[l];
+    const int first = w.level_start[l + 1] + (u - w.level_start[l]) * k;
+    const float *row = ssm + ((size_t)b * NQ + u) * V;
+    __shared__ float s_v[kExpandThreads / 32];
+    __shared__ int s_i[kExpandThreads / 32];
+    __shared__ int s_nf;
+    __shared__ float pick_v;
+    __shared__ int pick_i;
+    if (tid == 0) s_nf = 0;
+    float lv = INFINITY;
+    int li = -1;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        bool nf = false;
+        auto take = [&](float x, int i) {
+            if (r == 0 && !isfinite(x)) nf = true;
+            if ((x < lv || (x == lv && i > li)) && ranks_above(x, i, bv, bi)) { bv = x; bi = i; }
+        };
+        if (vec4) {
+            const float4 *r4 = reinterpret_cast<const float4 *>(row);
+            for (int g = tid; g < (V >> 2); g += kExpandThreads) {
+                const float4 a = __ldg(r4 + g);
+                take(a.x, 4 * g); take(a.y, 4 * g + 1); take(a.z, 4 * g + 2); take(a.w, 4 * g + 3);
+            }
+        } else {
+            for (int i = tid; i < V; i += kExpandThreads) take(__ldg(row + i), i);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        nf = __any_sync(0xffffffffu, nf);
+        if ((tid & 31) == 0) {
+            s_v[tid >> 5] = bv;
+            s_i[tid >> 5] = bi;
+            if (nf) s_nf = 1;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int q = 1; q < kExpandThreads / 32; ++q)
+                if (ranks_above(s_v[q], s_i[q], bv, bi)) { bv = s_v[q]; bi = s_i[q]; }
+            pick_v = bv;
+            pick_i = bi < V ? bi : -1;   // fewer than k tokens in the row
+        }
+        __syncthreads();
+        if (s_nf) {   // a non-finite drafter value: the children get no token
+            if (tid < k) tokens[(size_t)b * n_max + first + tid] = -1;
+            if (tid == 0) flag(status, TS_STATUS_NONFINITE);
+            return;
+        }
+        lv = pick_v;
+        li = pick_i;
+        if (tid == 0) tokens[(size_t)b * n_max + first + r] = li;
+        __syncthreads();   // pick_v / pick_i are rewritten by the next pass
+        if (li < 0) return;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
@@ -289,6 +375,14 @@ cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
     return launch(k_build_chains, dim3(t.B), dim3(kMaxNodes), 0, s, t, root_token, chains, C, len, tokens_out, p_row,
                   q_row, prefix_len, status);
+}
+
+cudaError_t launch_expand_topk(int32_t *tokens, const int32_t *root_token, const float *ssm, int NQ, int B,
+                              int n_max, const WidthsParam &w, int n_internal, int V, uint32_t *status,
+                              cudaStream_t s) {
+    const bool vec4 = (V % 4 == 0) && ((uintptr_t)ssm % 16 == 0);
+    return launch(k_expand_topk, dim3(n_internal, B), dim3(kExpandThreads), 0, s, tokens, root_token, ssm, NQ, w, V,
+                  n_max, vec4, status);
 }
 
 }  // namespace ts

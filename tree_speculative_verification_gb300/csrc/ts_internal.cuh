@@ -65,6 +65,10 @@ cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token
                                      int C, int len, int32_t *tokens_out, int32_t *p_row, int32_t *q_row,
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s);
 
+cudaError_t launch_expand_topk(int32_t *tokens, const int32_t *root_token, const float *ssm, int NQ, int B,
+                              int n_max, const WidthsParam &w, int n_internal, int V, uint32_t *status,
+                              cudaStream_t s);
+
 cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              int esize, uint32_t *status, cudaStream_t s);
