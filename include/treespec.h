@@ -99,6 +99,22 @@ typedef struct ts_tree {
 } ts_tree;
 
 /*
+ * A paged KV cache: keys (and values) live in pages of TS_PAGE_KEYS rows; page
+ * g holds, for every head h, rows [g][h][0..TS_PAGE_KEYS) of d values
+ * (layout [num_pages][H][TS_PAGE_KEYS][d], 16-byte aligned). Logical row r of
+ * request b is row r % TS_PAGE_KEYS of page block_table[b][r / TS_PAGE_KEYS].
+ * The pages of one request need not be contiguous or ordered; every page a
+ * request's rows 0 .. P + n - 1 touch must be listed, and distinct requests
+ * must not share the pages they write. Device pointers, owned by the caller.
+ */
+#define TS_PAGE_KEYS 64
+typedef struct ts_paged_kv {
+    void *k_pages, *v_pages;       /* [num_pages][H][TS_PAGE_KEYS][d] */
+    const int32_t *block_table;    /* [B][max_pages] page ids */
+    int32_t num_pages, max_pages;
+} ts_paged_kv;
+
+/*
  * tree_build -- depth-first linearisation (SpecInfer sec. 4.2 and Fig. 4;
  * expansion configuration of sec. 3 / Fig. 3; position ids = prefix length +
  * depth as on the "Speculative decoding" concept page, Implementation sketch).
@@ -284,6 +300,30 @@ ts_status kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len,
 ts_status tree_attention_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
                                  const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max,
                                  ts_dtype dtype, float scale, uint32_t *status, cudaStream_t stream);
+
+/*
+ * Paged-cache forms of kv_append, tree_attention and kv_commit (the shared
+ * tree cache of SpecInfer sec. 4.2 kept in pages, so requests of different
+ * lengths need no common L_max): the same operations, arguments and rules as
+ * the dense calls, with the cache given as a ts_paged_kv instead of
+ * (k_cache, v_cache, L_max). bf16 only (TS_ERR_UNSUPPORTED otherwise) and
+ * head_dim 128 or 64. tree_attention_paged runs the kernels tree_attention
+ * chooses (one 64-key tile is one page) except the small-tree tcgen05 kernel,
+ * whose 128-key tiles span two pages; its workspace is
+ * treespec_workspace_size(TS_OP_ATTENTION, B, H, n_max, d,
+ * max_pages * TS_PAGE_KEYS, V). A page id outside [0, num_pages) sets
+ * TS_STATUS_INDEX: tree_attention_paged reads zeros in its place (the
+ * request's outputs are then not meaningful), kv_append_paged and
+ * kv_commit_paged leave that request's pages unchanged.
+ */
+ts_status kv_append_paged(const ts_paged_kv *kv, const void *k_new, const void *v_new, const int32_t *prefix_len,
+                          const ts_tree *t, int H, int d, uint32_t *status, cudaStream_t stream);
+ts_status tree_attention_paged(void *out, const void *q, const ts_paged_kv *kv, const int32_t *prefix_len,
+                               const ts_tree *t, int H, int d, float scale, void *ws, size_t ws_bytes,
+                               uint32_t *status, cudaStream_t stream);
+ts_status kv_commit_paged(const ts_paged_kv *kv, const int32_t *prefix_len, int32_t *new_prefix_len,
+                          const int32_t *out_path, const int32_t *out_count, const ts_tree *t, int H, int d,
+                          uint32_t *status, cudaStream_t stream);
 
 /* Bytes of workspace an op needs for these sizes on the current device (0 if none). */
 size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_max, int V);

@@ -21,12 +21,13 @@ TS_F32, TS_BF16 = 0, 1
 TS_OP_ATTENTION, TS_OP_VERIFY_GREEDY, TS_OP_VERIFY_MSS = 0, 1, 2
 STATUS_BAD_TREE, STATUS_NONFINITE, STATUS_ZERO_RESID, STATUS_INDEX, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 MAX_NODES = 256
+PAGE_KEYS = 64   # TS_PAGE_KEYS
 
 #: every entry point of the C ABI (include/treespec.h)
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
            "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive",
-           "tree_expand_topk")
+           "tree_expand_topk", "kv_append_paged", "tree_attention_paged", "kv_commit_paged")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -39,6 +40,11 @@ class ts_tree(C.Structure):
     _fields_ = [("B", C.c_int32), ("n_max", C.c_int32)] + [
         (name, C.c_void_p) for name in ("n_nodes", "perm", "dfs_of", "parent", "token", "depth", "pos", "sub_end",
                                         "anc")]
+
+
+class ts_paged_kv(C.Structure):
+    _fields_ = [("k_pages", C.c_void_p), ("v_pages", C.c_void_p), ("block_table", C.c_void_p),
+                ("num_pages", C.c_int32), ("max_pages", C.c_int32)]
 
 
 _lib = None
@@ -65,6 +71,9 @@ def load_library(path: str | None = None):
         "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
         "verify_naive": [P, P, P, P, P, I, P, F, T, I, P, P],
         "tree_expand_topk": [P, P, P, I, I, I, P, I, I, P, P],
+        "kv_append_paged": [C.POINTER(ts_paged_kv), P, P, P, T, I, I, P, P],
+        "tree_attention_paged": [P, P, C.POINTER(ts_paged_kv), P, T, I, I, F, P, Z, P, P],
+        "kv_commit_paged": [C.POINTER(ts_paged_kv), P, P, P, P, T, I, I, P, P],
         "kv_commit": [P, P, P, P, P, P, T, I, I, I, I, P, P],
         "treespec_workspace_init": [P, Z, P],
         "tree_attention_noalloc": [P, P, P, P, P, T, I, I, I, I, F, P, P],
@@ -252,6 +261,49 @@ def kv_commit(k_cache, v_cache, prefix_len, new_prefix_len, out_path, out_count,
     _check(lib.kv_commit(_ptr(k_cache), _ptr(v_cache), _ptr(_i32(prefix_len, "prefix_len")),
                          _ptr(_i32(new_prefix_len, "new_prefix_len")), _ptr(out_path), _ptr(out_count), tree.c, H, d,
                          L_max, _dtype(k_cache), _ptr(status), _stream(stream)), "kv_commit")
+
+
+class PagedKV:
+    """A paged KV cache (the ts_paged_kv of the C ABI): k_pages / v_pages
+    [num_pages][H][PAGE_KEYS][d] bf16 and block_table [B][max_pages] int32."""
+
+    def __init__(self, k_pages, v_pages, block_table):
+        if k_pages.dtype != torch.bfloat16 or v_pages.shape != k_pages.shape:
+            raise TreespecError("pages must be two bf16 tensors of one shape [num_pages][H][64][d]")
+        if k_pages.shape[2] != PAGE_KEYS:
+            raise TreespecError(f"a page holds {PAGE_KEYS} keys")
+        self.k_pages, self.v_pages, self.block_table = k_pages, v_pages, _i32(block_table, "block_table")
+        self.H, self.d = k_pages.shape[1], k_pages.shape[3]
+        self._c = ts_paged_kv(k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(), k_pages.shape[0],
+                              block_table.shape[1])
+
+    @property
+    def c(self):
+        return C.byref(self._c)
+
+    @property
+    def L_max(self) -> int:
+        return self.block_table.shape[1] * PAGE_KEYS
+
+
+def kv_append_paged(kv: PagedKV, k_new, v_new, prefix_len, tree: Tree, status=None, stream=None):
+    _check(load_library().kv_append_paged(kv.c, _ptr(k_new), _ptr(v_new), _ptr(_i32(prefix_len, "prefix_len")), tree.c,
+                                          kv.H, kv.d, _ptr(status), _stream(stream)), "kv_append_paged")
+
+
+def tree_attention_paged(out, q, kv: PagedKV, prefix_len, tree: Tree, scale=0.0, ws=None, status=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load_library().tree_attention_paged(_ptr(out), _ptr(q), kv.c, _ptr(_i32(prefix_len, "prefix_len")), tree.c,
+                                               kv.H, kv.d, float(scale), _ptr(ws), nbytes, _ptr(status),
+                                               _stream(stream)), "tree_attention_paged")
+
+
+def kv_commit_paged(kv: PagedKV, prefix_len, new_prefix_len, out_path, out_count, tree: Tree, status=None,
+                    stream=None):
+    _check(load_library().kv_commit_paged(kv.c, _ptr(_i32(prefix_len, "prefix_len")),
+                                          _ptr(_i32(new_prefix_len, "new_prefix_len")), _ptr(out_path),
+                                          _ptr(out_count), tree.c, kv.H, kv.d, _ptr(status), _stream(stream)),
+           "kv_commit_paged")
 
 
 def version() -> str:

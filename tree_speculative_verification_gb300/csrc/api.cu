@@ -280,6 +280,75 @@ ts_status kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int
                        "kv_commit");
 }
 
+// ---- paged cache -------------------------------------------------------------
+static ts_status check_paged(const ts_paged_kv *kv, const ts_tree *t, int H, int d, const char *who) {
+    if (!kv || !kv->k_pages || !kv->v_pages || !kv->block_table) return fail(TS_ERR_INVALID_ARG, "%s: NULL cache", who);
+    if (kv->num_pages < 1 || kv->max_pages < 1)
+        return fail(TS_ERR_INVALID_ARG, "%s: num_pages=%d, max_pages=%d", who, kv->num_pages, kv->max_pages);
+    if ((long long)kv->num_pages * H * TS_PAGE_KEYS >= (1LL << 31))
+        return fail(TS_ERR_INVALID_ARG, "%s: 2^31 cache rows or more", who);
+    if (!aligned16(kv->k_pages) || !aligned16(kv->v_pages))
+        return fail(TS_ERR_INVALID_ARG, "%s: pages must be 16-byte aligned", who);
+    return check_attn_shape(who, t, H, d, kv->max_pages * TS_PAGE_KEYS, TS_BF16);
+}
+
+static ts::PagedArgs paged_args(const ts_paged_kv *kv) {
+    ts::PagedArgs pg;
+    pg.bt = kv->block_table;
+    pg.max_pages = kv->max_pages;
+    pg.num_pages = kv->num_pages;
+    return pg;
+}
+
+ts_status kv_append_paged(const ts_paged_kv *kv, const void *k_new, const void *v_new, const int32_t *prefix_len,
+                          const ts_tree *t, int H, int d, uint32_t *status, cudaStream_t stream) {
+    ts_status st = check_tree(t, "kv_append_paged");
+    if (st || (st = check_paged(kv, t, H, d, "kv_append_paged"))) return st;
+    if (!k_new || !v_new || !prefix_len) return fail(TS_ERR_INVALID_ARG, "kv_append_paged: NULL pointer");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(TS_ERR_INVALID_ARG, "kv_append_paged: k_new and v_new must be 16-byte aligned");
+    return cuda_result(ts::launch_kv_append(kv->k_pages, kv->v_pages, k_new, v_new, prefix_len, *t, H, d,
+                                            kv->max_pages * TS_PAGE_KEYS, 2, status, stream, paged_args(kv)),
+                       "kv_append_paged");
+}
+
+ts_status tree_attention_paged(void *out, const void *q, const ts_paged_kv *kv, const int32_t *prefix_len,
+                               const ts_tree *t, int H, int d, float scale, void *ws, size_t ws_bytes,
+                               uint32_t *status, cudaStream_t stream) {
+    ts_status st = check_tree(t, "tree_attention_paged");
+    if (st || (st = check_paged(kv, t, H, d, "tree_attention_paged"))) return st;
+    if (!out || !q || !prefix_len) return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: NULL pointer");
+    if (!aligned16(out) || !aligned16(q))
+        return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: q and out must be 16-byte aligned");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    const int L_max = kv->max_pages * TS_PAGE_KEYS;
+    const ts::AttnPlan plan = ts::attn_plan(t->B, H, t->n_max, d, L_max, TS_BF16, false);
+    if (!ws || ws_bytes < plan.ws_bytes)
+        return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: workspace of %zu bytes needed, %zu given",
+                    plan.ws_bytes, ws ? ws_bytes : (size_t)0);
+    if (!aligned16(ws)) return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: workspace must be 16-byte aligned");
+    const char *why = nullptr;
+    cudaError_t e = ts::launch_attn_bf16(out, q, kv->k_pages, kv->v_pages, prefix_len, *t, H, d, L_max, scale, plan,
+                                         ws, status, stream, &why, paged_args(kv));
+    if (why) return fail(TS_ERR_CUDA, "tree_attention_paged: %s", why);
+    return cuda_result(e, "tree_attention_paged");
+}
+
+ts_status kv_commit_paged(const ts_paged_kv *kv, const int32_t *prefix_len, int32_t *new_prefix_len,
+                          const int32_t *out_path, const int32_t *out_count, const ts_tree *t, int H, int d,
+                          uint32_t *status, cudaStream_t stream) {
+    ts_status st = check_tree(t, "kv_commit_paged");
+    if (st || (st = check_paged(kv, t, H, d, "kv_commit_paged"))) return st;
+    if (!prefix_len || !new_prefix_len || !out_path || !out_count)
+        return fail(TS_ERR_INVALID_ARG, "kv_commit_paged: NULL pointer");
+    if (new_prefix_len == prefix_len)
+        return fail(TS_ERR_INVALID_ARG, "kv_commit_paged: new_prefix_len aliases prefix_len");
+    return cuda_result(ts::launch_kv_commit(kv->k_pages, kv->v_pages, prefix_len, new_prefix_len, out_path, out_count,
+                                            *t, H, d, kv->max_pages * TS_PAGE_KEYS, 2, status, stream,
+                                            paged_args(kv)),
+                       "kv_commit_paged");
+}
+
 size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_max, int V) {
     if (B < 1 || n_max < 1 || n_max > TS_MAX_NODES) return 0;
     switch (op) {

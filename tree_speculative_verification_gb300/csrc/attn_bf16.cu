@@ -201,7 +201,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
     if (sidx >= S_b) return;
     const int k_begin = sidx * chunk_keys, k_end = min(L, k_begin + chunk_keys);
     const int ntiles = (k_end - k_begin + TK - 1) / TK;
-    const int row0 = (b * a.H + h) * a.L_max + k_begin;
     const uint32_t bar0 = sm_base + C::OFF_BAR;
 
     if (tid == 0) {
@@ -213,19 +212,27 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
-    auto issue = [&](int it) {
+    static_assert(TK == TS_PAGE_KEYS, "one key tile is one page");
+    auto issue = [&](int it, int row) {
         const int st = it % STAGES;
         const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
         const uint32_t bar = bar0 + 8 * st;
         mbar_expect_tx(bar, C::STAGE_BYTES);
 #pragma unroll
         for (int bx = 0; bx < C::BOXES; ++bx) {
-            tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row0 + it * TK, bar);
-            tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row0 + it * TK, bar);
+            tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, bar);
+            tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, bar);
         }
     };
-    if (tid == 0)
-        for (int it = 0; it < min(STAGES, ntiles); ++it) issue(it);
+    if (tid == 0) {
+        int rows[STAGES];
+#pragma unroll
+        for (int it = 0; it < STAGES; ++it)   // every page id in flight before the first use
+            if (it < ntiles) rows[it] = tile_row(a, b, h, k_begin + it * TK);
+#pragma unroll
+        for (int it = 0; it < STAGES; ++it)
+            if (it < ntiles) issue(it, rows[it]);
+    }
 
     // Q rows of the CTA's nodes (DFS order) into swizzled shared memory; ancestor masks
     const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
@@ -291,6 +298,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % STAGES;
         const uint32_t phase = (uint32_t)(it / STAGES) & 1u;
+        // the row of the tile issued at the end of this iteration, fetched now
+        const int next_row = (tid == 0 && it + STAGES < ntiles) ? tile_row(a, b, h, k_begin + (it + STAGES) * TK) : 0;
         if (!mbar_wait_bounded(bar0 + 8 * st, phase)) { timed_out = 1; break; }
         const int key_base = k_begin + it * TK;
         unsigned char *ktile = sm + st * C::STAGE_BYTES;
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
         if (lane == 0) mbar_arrive(ebar0 + 8 * st);
         if (tid == 0 && it + STAGES < ntiles) {
             if (!mbar_wait_bounded(ebar0 + 8 * st, phase)) { timed_out = 1; break; }
-            issue(it + STAGES);
+            issue(it + STAGES, next_row);
         }
     }
     if (__syncthreads_or(timed_out)) {
@@ -622,7 +631,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     if (sidx >= S_b) return;
     const int k_begin = sidx * chunk_keys, k_end = min(L, k_begin + chunk_keys);
     const int ntiles = (k_end - k_begin + C::TKT - 1) / C::TKT;
-    const int row0 = (b * a.H + h) * a.L_max + k_begin;
 
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
     const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
@@ -686,6 +694,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
         if (lane == 0) {   // ---------------------------------------------- TMA producer
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % C::STAGES;
+                const int row = tile_row(a, b, h, k_begin + j * C::TKT);   // fetched before the wait
                 if (j >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((j / C::STAGES) - 1) & 1u)) {
                     misc[1] = 1;
                     break;
@@ -694,8 +703,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
                 mbar_expect_tx(full + 8 * st, C::STAGE_BYTES);
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx) {
-                    tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row0 + j * C::TKT, full + 8 * st);
-                    tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row0 + j * C::TKT, full + 8 * st);
+                    tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, full + 8 * st);
+                    tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, full + 8 * st);
                 }
             }
         }
@@ -1025,9 +1034,9 @@ __global__ void __launch_bounds__(TpCfg::THREADS, 1) k_attn_tp(const __grid_cons
             bool ok = true;
             for (int p = blockIdx.x; p < pairs && ok; p += G) {
                 const ItemInfo it = item_info(a, p);
-                const int row0 = p * a.L_max;
                 for (int j = 0; j < it.ntiles; ++j, ++g) {
                     const int st = g % C::STAGES;
+                    const int row = tile_row(a, p / a.H, p % a.H, j * C::TKT);   // fetched before the wait
                     if (g >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((g / C::STAGES) - 1) & 1u)) {
                         ok = false;
                         break;
@@ -1036,8 +1045,8 @@ __global__ void __launch_bounds__(TpCfg::THREADS, 1) k_attn_tp(const __grid_cons
                     mbar_expect_tx(full + 8 * st, C::STAGE_BYTES);
 #pragma unroll
                     for (int bx = 0; bx < 2; ++bx) {
-                        tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row0 + j * C::TKT, full + 8 * st);
-                        tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row0 + j * C::TKT, full + 8 * st);
+                        tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, full + 8 * st);
+                        tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, full + 8 * st);
                     }
                 }
             }
@@ -1437,10 +1446,10 @@ int num_sms() {
     return n > 0 ? n : 152;
 }
 
-AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool allow_small_tree) {
     AttnPlan p{1, 1, 0, 0, false, false, "k_attn_f32"};
     if (dt != TS_BF16) return p;
-    if (use_kt(d, n_max)) {
+    if (allow_small_tree && use_kt(d, n_max)) {
         p.n_pad = 32;
         p.small_tree = true;
         p.kernel = "k_attn_kt";
@@ -1484,12 +1493,14 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
 
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max, float scale,
-                             const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s, const char **why) {
+                             const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s, const char **why,
+                             const PagedArgs &pg) {
     if (plan.small_tree)
         return launch_attn_kt(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, ws, status, s, why);
     const Variant v = pick_variant(d, t.n_max);
     CUtensorMap mk, mv;
-    const long long rows = (long long)t.B * H * L_max;
+    // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
+    const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
     if (!make_map(&mk, k_cache, d, rows, TK) || !make_map(&mv, v_cache, d, rows, TK)) {
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
@@ -1513,6 +1524,9 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
     a.part_ml = (float *)((char *)ws + counters);
     a.part_o = a.part_ml + pairs * plan.splits * 2 * plan.n_pad;
     a.status = status;
+    a.bt = pg.bt;
+    a.max_pages = pg.max_pages;
+    a.num_pages = pg.num_pages;
     if (plan.persistent) {
         e = cudaFuncSetAttribute(k_attn_tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpCfg::SMEM);
         if (e != cudaSuccess) return e;

@@ -102,7 +102,23 @@ struct AttnArgs {
     float *part_ml;   // [B*H*splits][2][n_pad]
     float *part_o;    // [B*H*splits][n_pad][D]
     uint32_t *status;
+    const int32_t *bt = nullptr;   // paged cache: block table [B][max_pages], else dense
+    int max_pages = 0, num_pages = 0;
 };
+
+// TMA row of the 64-key tile that starts at logical key key0 of (b, h): the
+// dense strip [b][h][L_max], or the tile's page ([page][H][64]). A page id
+// outside the table sets TS_STATUS_INDEX and points the load far past the
+// tensor, where TMA fills zeros.
+__device__ __forceinline__ int tile_row(const AttnArgs &a, int b, int h, int key0) {
+    if (!a.bt) return (b * a.H + h) * a.L_max + key0;
+    const int page = __ldg(a.bt + (size_t)b * a.max_pages + key0 / TS_PAGE_KEYS);
+    if (page < 0 || page >= a.num_pages) {
+        flag(a.status, TS_STATUS_INDEX);
+        return 0x40000000;
+    }
+    return (page * a.H + h) * TS_PAGE_KEYS;
+}
 
 // ------------------------------------------------------------- tcgen05 ---
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {

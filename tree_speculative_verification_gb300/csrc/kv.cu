@@ -16,7 +16,8 @@ constexpr int kKvThreads = 256;
 // four independent copies in flight per thread.
 __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 *v_cache, const uint4 *k_new,
                                                           const uint4 *v_new, const int32_t *prefix_len, ts_tree t,
-                                                          int H, int row_vec, int L_max, uint32_t *status) {
+                                                          int H, int row_vec, int L_max, uint32_t *status,
+                                                          PagedArgs pg) {
     const int b = blockIdx.y, h = blockIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -26,10 +27,20 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 
         if (h == 0 && threadIdx.x == 0) flag(status, TS_STATUS_INDEX);
         return;
     }
-    __shared__ int dfs_s[kMaxNodes];
-    for (int v = threadIdx.x; v < n; v += kKvThreads) dfs_s[v] = t.dfs_of[(size_t)b * t.n_max + v];
+    // cache row of every node (row P + its depth-first index)
+    __shared__ long long dst_s[kMaxNodes];
+    __shared__ int bad_s;
+    if (threadIdx.x == 0) bad_s = 0;
     __syncthreads();
-    const size_t cache_base = ((size_t)b * H + h) * L_max + P;
+    for (int v = threadIdx.x; v < n; v += kKvThreads) {
+        dst_s[v] = cache_row(pg, b, h, H, L_max, P + t.dfs_of[(size_t)b * t.n_max + v]);
+        if (dst_s[v] < 0) bad_s = 1;
+    }
+    __syncthreads();
+    if (bad_s) {
+        if (h == 0 && threadIdx.x == 0) flag(status, TS_STATUS_INDEX);
+        return;
+    }
     const int total = n * row_vec;
     for (int base = threadIdx.x; base < total; base += 4 * kKvThreads) {
         uint4 kv[4], vv[4];
@@ -40,7 +51,7 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 
             if (idx < total) {
                 const int v = idx / row_vec, c = idx - v * row_vec;
                 const size_t src = (((size_t)b * t.n_max + v) * H + h) * row_vec + c;
-                dst[k] = (cache_base + dfs_s[v]) * row_vec + c;
+                dst[k] = (size_t)dst_s[v] * row_vec + c;
                 kv[k] = __ldcs(k_new + src);
                 vv[k] = __ldcs(v_new + src);
             }
@@ -62,7 +73,7 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 
 __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 *v_cache, const int32_t *prefix_len,
                                                           int32_t *new_prefix_len, const int32_t *out_path,
                                                           const int32_t *out_count, ts_tree t, int H, int row_vec,
-                                                          int L_max, uint32_t *status) {
+                                                          int L_max, uint32_t *status, PagedArgs pg) {
     const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -87,7 +98,21 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 
         }
         return;
     }
-    const size_t base = ((size_t)b * H + h) * L_max + P;
+    // cache rows of the moves: source P + dfs(path[i]), destination P + i
+    __shared__ long long from_s[kMaxNodes + 1], to_s[kMaxNodes + 1];
+    if (tid < cnt) {
+        from_s[tid] = cache_row(pg, b, h, H, L_max, P + src_s[tid]);
+        to_s[tid] = cache_row(pg, b, h, H, L_max, P + tid);
+        if (from_s[tid] < 0 || to_s[tid] < 0) bad_s = 1;
+    }
+    __syncthreads();
+    if (bad_s) {
+        if (h == 0 && tid == 0) {
+            flag(status, TS_STATUS_INDEX);
+            new_prefix_len[b] = P;
+        }
+        return;
+    }
     const int total = cnt * row_vec;
     for (int r0 = 0; r0 < total; r0 += kKvThreads) {
         const int idx = r0 + tid;
@@ -97,13 +122,13 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 
         if (mine) {
             i = idx / row_vec;
             c = idx - i * row_vec;
-            kx = k_cache[(base + src_s[i]) * row_vec + c];
-            vx = v_cache[(base + src_s[i]) * row_vec + c];
+            kx = k_cache[(size_t)from_s[i] * row_vec + c];
+            vx = v_cache[(size_t)from_s[i] * row_vec + c];
         }
         __syncthreads();
         if (mine && src_s[i] != i) {
-            k_cache[(base + i) * row_vec + c] = kx;
-            v_cache[(base + i) * row_vec + c] = vx;
+            k_cache[(size_t)to_s[i] * row_vec + c] = kx;
+            v_cache[(size_t)to_s[i] * row_vec + c] = vx;
         }
         __syncthreads();
     }
@@ -114,20 +139,20 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 
 
 cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max, int esize,
-                             uint32_t *status, cudaStream_t s) {
+                             uint32_t *status, cudaStream_t s, const PagedArgs &pg) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
     return launch(k_kv_append, grid, dim3(kKvThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new,
-                  (const uint4 *)v_new, prefix_len, t, H, row_vec, L_max, status);
+                  (const uint4 *)v_new, prefix_len, t, H, row_vec, L_max, status, pg);
 }
 
 cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int32_t *new_prefix_len,
                              const int32_t *out_path, const int32_t *out_count, const ts_tree &t, int H, int d,
-                             int L_max, int esize, uint32_t *status, cudaStream_t s) {
+                             int L_max, int esize, uint32_t *status, cudaStream_t s, const PagedArgs &pg) {
     const int row_vec = d * esize / 16;
     dim3 grid(H, t.B);
     return launch(k_kv_commit, grid, dim3(kKvThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, prefix_len,
-                  new_prefix_len, out_path, out_count, t, H, row_vec, L_max, status);
+                  new_prefix_len, out_path, out_count, t, H, row_vec, L_max, status, pg);
 }
 
 }  // namespace ts

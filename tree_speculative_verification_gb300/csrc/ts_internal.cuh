@@ -69,12 +69,28 @@ cudaError_t launch_expand_topk(int32_t *tokens, const int32_t *root_token, const
                               int n_max, const WidthsParam &w, int n_internal, int V, uint32_t *status,
                               cudaStream_t s);
 
+// Row addressing of the KV cache: dense [B][H][L_max][d] when bt is null, else
+// pages of TS_PAGE_KEYS rows ([page][H][TS_PAGE_KEYS][d]) listed per request in
+// bt [B][max_pages]. Returns the cache row of (b, h, logical row r), or -1 for
+// a page id outside [0, num_pages).
+struct PagedArgs {
+    const int32_t *bt = nullptr;
+    int max_pages = 0, num_pages = 0;
+};
+__device__ __forceinline__ long long cache_row(const PagedArgs &pg, int b, int h, int H, int L_max, int r) {
+    if (!pg.bt) return ((long long)b * H + h) * L_max + r;
+    const int page = pg.bt[(size_t)b * pg.max_pages + r / TS_PAGE_KEYS];
+    if (page < 0 || page >= pg.num_pages) return -1;
+    return ((long long)page * H + h) * TS_PAGE_KEYS + r % TS_PAGE_KEYS;
+}
+
 cudaError_t launch_kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
-                             int esize, uint32_t *status, cudaStream_t s);
+                             int esize, uint32_t *status, cudaStream_t s, const PagedArgs &pg = PagedArgs());
 cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix_len, int32_t *new_prefix_len,
                              const int32_t *out_path, const int32_t *out_count, const ts_tree &t, int H,
-                             int d, int L_max, int esize, uint32_t *status, cudaStream_t s);
+                             int d, int L_max, int esize, uint32_t *status, cudaStream_t s,
+                             const PagedArgs &pg = PagedArgs());
 
 // Split-KV plan shared by the size query and the launch.
 struct AttnPlan {
@@ -86,7 +102,7 @@ struct AttnPlan {
     bool small_tree;   // the small-tree tcgen05 kernel (key tiles cut evenly over the SMs)
     const char *kernel;  // name of the kernel the launch uses
 };
-AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool allow_small_tree = true);
 
 cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, const float *v_cache,
                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
@@ -100,7 +116,7 @@ cudaError_t launch_attn_kt(void *out, const void *q, const void *k_cache, const 
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,
-                             const char **why);
+                             const char **why, const PagedArgs &pg = PagedArgs());
 
 size_t greedy_ws_bytes(int B, int n_max, int V);
 cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
