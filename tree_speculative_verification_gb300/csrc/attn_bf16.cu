@@ -16,6 +16,9 @@
 //    side and the few tree nodes (8 per n-tile) on the N side, so a 21-node
 //    tree pads to 24 columns, not 32 rows. P^T is moved from the accumulator
 //    layout to the B-operand layout with movmatrix; O^T = V^T P^T.
+//  * With ragged prefixes the grid rows take the requests longest first (the
+//    rank of P_b + n_b, computed by every CTA from the B counts), so that the
+//    longest (request, head) pairs start in the first wave of CTAs.
 //  * Online softmax per node column in the exp2 domain; the CTA's partial
 //    (max, sum, O) goes to the workspace and the last CTA of the (request,
 //    head) -- found with an atomic counter, no waiting -- merges the splits.
@@ -185,10 +188,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp / KS, ks = warp % KS;
     const int g = lane >> 2, tq = lane & 3;
-    const int b = blockIdx.y, h = blockIdx.x, sidx = blockIdx.z;
+    const int h = blockIdx.x, sidx = blockIdx.z;
     const ts_tree &t = a.t;
     pdl_wait();
     pdl_trigger();
+    const int b = request_by_rank(a, blockIdx.y, (int *)(sm + C::OFF_Q));
     const int n = t.n_nodes[b], P = a.prefix_len[b];
     if (n <= 0) return;
     if (P < 0 || P + n > a.L_max) {
@@ -1527,6 +1531,9 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
     a.bt = pg.bt;
     a.max_pages = pg.max_pages;
     a.num_pages = pg.num_pages;
+    // longest-first dispatch of the requests (TREESPEC_ATTN_LPT=0: request order)
+    const char *lp = getenv("TREESPEC_ATTN_LPT");
+    a.lpt = !(lp && *lp && atoi(lp) == 0);
     if (plan.persistent) {
         e = cudaFuncSetAttribute(k_attn_tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpCfg::SMEM);
         if (e != cudaSuccess) return e;

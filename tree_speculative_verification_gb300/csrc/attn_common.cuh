@@ -104,6 +104,7 @@ struct AttnArgs {
     uint32_t *status;
     const int32_t *bt = nullptr;   // paged cache: block table [B][max_pages], else dense
     int max_pages = 0, num_pages = 0;
+    int lpt = 0;                   // grid rows take requests longest first
 };
 
 // TMA row of the 64-key tile that starts at logical key key0 of (b, h): the
@@ -118,6 +119,33 @@ __device__ __forceinline__ int tile_row(const AttnArgs &a, int b, int h, int key
         return 0x40000000;
     }
     return (page * a.H + h) * TS_PAGE_KEYS;
+}
+
+// Longest-first dispatch: grid row r is given the request with the r-th
+// largest key count P_b + n_b (ties to the lower index), so with ragged
+// prefixes the longest (request, head) pairs start in the first wave of CTAs
+// and the short ones fill the tail. The order is a permutation whatever the
+// values (a strict total order on (count desc, index asc)). Requests beyond
+// blockDim.x keep their own row. Called by every thread before any early
+// return; s holds blockDim.x + 1 ints of shared scratch.
+__device__ __forceinline__ int request_by_rank(const AttnArgs &a, int r, int *s) {
+    const int B = a.t.B, tid = threadIdx.x;
+    if (!a.lpt || B > (int)blockDim.x) return r;
+    if (tid < B) s[tid] = a.t.n_nodes[tid] + a.prefix_len[tid];
+    __syncthreads();
+    if (tid < B) {
+        const int mine = s[tid];
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            const int o = s[j];
+            rank += (o > mine) | ((o == mine) & (j < tid));
+        }
+        if (rank == r) s[blockDim.x] = tid;
+    }
+    __syncthreads();
+    const int b = s[blockDim.x];
+    __syncthreads();   // the scratch may be reused after this
+    return b;
 }
 
 // ------------------------------------------------------------- tcgen05 ---
