@@ -87,8 +87,11 @@ def _random_paths(rng, par, B, n):
     return op, oc
 
 
-@pytest.mark.parametrize("mode,n", [("mma", 21), ("splits", 21), ("tc", 40), ("persistent", 40), ("mma", 150)])
+@pytest.mark.parametrize("mode,n", [("mma", 21), ("splits", 21), ("tc", 40), ("persistent", 40), ("mma", 150),
+                                    ("tq", 40), ("tq", 100)])
 def test_paged_equals_dense(mode, n, monkeypatch):
+    if mode == "tq":
+        monkeypatch.setenv("TREESPEC_ATTN_KERNEL", "tq")
     if mode in ("mma", "splits"):
         monkeypatch.setenv("TREESPEC_ATTN_KERNEL", "mma")
     if mode == "splits":

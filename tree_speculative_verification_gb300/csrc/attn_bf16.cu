@@ -585,25 +585,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
 // bounded; TMEM is freed on every exit path.
 // ============================================================================
 struct TcCfg {
-    static constexpr int D = 128, TKT = 64, STAGES = 4, NODES = 128, STREAMS = 2;
+    static constexpr int D = 128, TKT = 64, STAGES = 6, NODES = 128, STREAMS = 2;
     static constexpr int THREADS = 64 + STREAMS * 128;
     static constexpr int BOX_BYTES = TKT * 128;           // 64 key rows x 128 bytes
     static constexpr int TILE_BYTES = 2 * BOX_BYTES;      // K (or V) of 64 keys x 128 dims
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
-    static constexpr int QBOX = NODES * 128;              // 128 node rows x 64 dims
-    static constexpr int Q_BYTES = 2 * QBOX;
-    static constexpr int P_BYTES = NODES * 128;           // 128 node rows x 64 keys, one per stream
     static constexpr int ANC_WORDS = 4;                   // 128 nodes
-    static constexpr int OFF_Q = STAGES * STAGE_BYTES;
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;
-    static constexpr int OFF_ANC = OFF_P + STREAMS * P_BYTES;
+    static constexpr int OFF_ANC = STAGES * STAGE_BYTES;
     static constexpr int OFF_PERM = OFF_ANC + NODES * ANC_WORDS * 4;
     static constexpr int OFF_ML = OFF_PERM + NODES * 4;   // stream 1's (max, sum) per row for the merge
-    static constexpr int NBAR = 2 * STAGES + 4 * STREAMS + 1;
+    static constexpr int NBAR = 2 * STAGES + 4 * STREAMS + 2;
     static constexpr int OFF_BAR = OFF_ML + NODES * 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = 512;            // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
+    // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384), Q [384,448)
+    // (bf16 pairs), P0 [448,480) P1 [480,512) (bf16 pairs)
+    static constexpr uint32_t TMEM_COLS = 512, Q_COL = 384, P_COL = 448;
 };
 
 __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_constant__ CUtensorMap map_k,
@@ -639,7 +636,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
     const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
     const uint32_t pfull = sfree + 8 * C::STREAMS, pvdone = pfull + 8 * C::STREAMS;
-    const uint32_t fin = pvdone + 8 * C::STREAMS;
+    const uint32_t fin = pvdone + 8 * C::STREAMS, qready = fin + 8;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
@@ -659,40 +656,45 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
             mbar_init(pvdone + 8 * x, 1);
         }
         mbar_init(fin, 1);
+        mbar_init(qready, 4);
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // Q rows (DFS order) in the 128-byte swizzled K-major layout; zero rows past n
     const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
     for (int r = tid; r < C::NODES; r += C::THREADS) perm_s[r] = r < n ? t.perm[(size_t)b * n_max + r] : -1;
-    __syncthreads();
-    {
-        // every Q load of a thread issued before any of its stores
-        constexpr int PER = (C::NODES * 16 + C::THREADS - 1) / C::THREADS;
-        uint4 qv[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int idx = tid + k * C::THREADS, r = idx >> 4, c = idx & 15;
-            qv[k] = make_uint4(0u, 0u, 0u, 0u);
-            if (idx < C::NODES * 16 && r < n)
-                qv[k] = __ldg((const uint4 *)(a.q + (((size_t)b * n_max + perm_s[r]) * a.H + h) * D) + c);
-        }
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-            const int idx = tid + k * C::THREADS, r = idx >> 4, c = idx & 15;
-            if (idx < C::NODES * 16)
-                *(uint4 *)(sm + C::OFF_Q + (c >> 3) * C::QBOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = qv[k];
-        }
-    }
     for (int idx = tid; idx < C::NODES * C::ANC_WORDS; idx += C::THREADS) {
         const int r = idx / C::ANC_WORDS, w = idx % C::ANC_WORDS;
         anc_s[idx] = (r < n && w < W) ? t.anc[((size_t)b * n_max + r) * W + w] : 0u;
     }
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = (uint32_t)misc[0];
+    if (warp >= 2 && warp < 6) {
+        // Q rows (DFS order) into TMEM as the S MMA's A operand: lane = node row,
+        // column c = dims 2c, 2c+1; zero rows past n. Stream 0's four warps
+        // cover the four lane quarters.
+        const int row = (warp & 3) * 32 + lane;
+        const uint4 *src = row < n ? (const uint4 *)(a.q + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D) : nullptr;
+        const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::Q_COL;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t qw[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const uint4 v = src ? __ldg(src + half * 8 + c4) : make_uint4(0u, 0u, 0u, 0u);
+                qw[4 * c4] = v.x;
+                qw[4 * c4 + 1] = v.y;
+                qw[4 * c4 + 2] = v.z;
+                qw[4 * c4 + 3] = v.w;
+            }
+            tc_st32u(tq + half * 32, qw);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qready);
+    }
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------------- TMA producer
@@ -717,7 +719,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
         if (lane == 0) {   // ---------------------------------------------- MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
-            const uint32_t q_base = sm_base + C::OFF_Q;
             // S of tile j into stream (j & 1)'s score buffer
             auto issue_s = [&](int j) -> bool {
                 const int st = j % C::STAGES, x = j & 1, k = j >> 1;
@@ -727,26 +728,26 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
                 const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(q_base + (kk >> 2) * C::QBOX + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    tc_mma(tmem + x * C::TKT, ad, bd, idesc_s, kk > 0);
+                    tc_mma_ts(tmem + x * C::TKT, tmem + C::Q_COL + kk * 8, bd, idesc_s, kk > 0);
                 }
                 tc_commit(sfull + 8 * x);
                 return true;
             };
-            bool ok = issue_s(0);
+            bool ok = mbar_wait_bounded(qready, 0);   // Q is in TMEM
+            tc_fence_after();
+            ok = ok && issue_s(0);
             for (int j = 0; j < ntiles && ok; ++j) {
                 if (j + 1 < ntiles && !(ok = issue_s(j + 1))) break;
                 const int x = j & 1, k = j >> 1, st = j % C::STAGES;
                 if (!mbar_wait_bounded(pfull + 8 * x, (uint32_t)k & 1u)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t pbase = sm_base + C::OFF_P + x * C::P_BYTES;
                 const uint32_t vbase = sm_base + st * C::STAGE_BYTES + C::TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < C::TKT / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
-                    tc_mma(tmem + 2 * C::TKT + x * D, ad, bd, idesc_pv, (k > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + 2 * C::TKT + x * D, tmem + C::P_COL + x * 32 + kk * 8, bd, idesc_pv,
+                              (k > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(empty + 8 * st);
                 tc_commit(pvdone + 8 * x);
@@ -849,13 +850,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
                 }
                 fence_async_smem();
             }
-            if (active) {
-                unsigned char *prow = sm + C::OFF_P + x * C::P_BYTES + row * 128;
-#pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16)
-                    *(uint4 *)(prow + ((c16 ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-                fence_async_smem();
+            if (active) {   // P (bf16 pairs) into this stream's TMEM columns: the PV MMA's A operand
+                tc_st32u(tl + C::P_COL + x * 32, pk);
+                tc_wait_st();
             }
             tc_fence_before();
             __syncwarp();
@@ -876,43 +873,44 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_cons
             const float f0 = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
             const float f1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
             const float lsum = l_run * f0 + m1.y * f1;
-            float o[D];
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
+            if (row < n && S_b > 1) {
+                a.part_ml[ps * 2 * a.n_pad + row] = M;
+                a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = lsum;
+            }
+            uint4 *dst = row < n && S_b == 1 ? (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D)
+                                             : nullptr;
+            float4 *po = row < n && S_b > 1 ? (float4 *)(a.part_o + (ps * a.n_pad + row) * D) : nullptr;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc_ld32(tl + 2 * C::TKT + q4 * 32, *reinterpret_cast<float(*)[32]>(&o[q4 * 32]));
-            tc_wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
+                float o[32];
+                tc_ld32(tl + 2 * C::TKT + q4 * 32, o);
+                tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < D; ++e) o[e] *= f0;
-            if (ntiles >= 2) {   // stream 1 wrote O1 (rows it never saw hold zeros there); CTA-uniform
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int e = 0; e < 32; ++e) o[e] *= f0;
+                if (ntiles >= 2) {   // stream 1 wrote O1 (rows it never saw hold zeros there); CTA-uniform
                     float o1[32];
                     tc_ld32(tl + 2 * C::TKT + D + q4 * 32, o1);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[q4 * 32 + e] = __fmaf_rn(o1[e], f1, o[q4 * 32 + e]);
+                    for (int e = 0; e < 32; ++e) o[e] = __fmaf_rn(o1[e], f1, o[e]);
                 }
-            }
-            if (row < n) {
-                if (S_b == 1) {
-                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                    uint4 *dst = (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D);
+                if (dst) {
 #pragma unroll
-                    for (int c16 = 0; c16 < D / 8; ++c16) {
-                        float dummy0, dummy1;
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float d0, d1;
                         uint4 v;
-                        v.x = pack_bf16(o[8 * c16] * inv, o[8 * c16 + 1] * inv, dummy0, dummy1);
-                        v.y = pack_bf16(o[8 * c16 + 2] * inv, o[8 * c16 + 3] * inv, dummy0, dummy1);
-                        v.z = pack_bf16(o[8 * c16 + 4] * inv, o[8 * c16 + 5] * inv, dummy0, dummy1);
-                        v.w = pack_bf16(o[8 * c16 + 6] * inv, o[8 * c16 + 7] * inv, dummy0, dummy1);
-                        dst[c16] = v;
+                        v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
+                        v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
+                        v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
+                        v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
+                        dst[q4 * 4 + c8] = v;
                     }
-                } else {
-                    const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
-                    a.part_ml[ps * 2 * a.n_pad + row] = M;
-                    a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = lsum;
-                    float4 *po = (float4 *)(a.part_o + (ps * a.n_pad + row) * D);
+                } else if (po) {
 #pragma unroll
-                    for (int c4 = 0; c4 < D / 4; ++c4) po[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        po[q4 * 8 + c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
                 }
             }
         }
@@ -1401,10 +1399,12 @@ cudaError_t launch_tc(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, c
     return launch(k_attn_tc, grid, dim3(TcCfg::THREADS), TcCfg::SMEM, s, mk, mv, a);
 }
 
-// Kernel choice for head_dim 128: trees of 33..128 nodes go to the 128-row
-// tcgen05 kernel, all others (and head_dim 64) to the mma.sync kernel.
-// TREESPEC_ATTN_KERNEL=mma, tc or kt forces one of them where its limits
-// allow; kt is the small-tree tcgen05 kernel (at most 32 nodes, keys on the
+// Kernel choice for head_dim 128: trees of 33..128 nodes go to the persistent
+// 128-key-tile tcgen05 kernel (k_attn_tq, attn_tq.cu), all others (and
+// head_dim 64) to the mma.sync kernel. TREESPEC_ATTN_KERNEL=mma, tq, tc or kt
+// forces one of them where its limits allow; tc is the earlier 64-key-tile
+// tcgen05 kernel (two softmax streams; with TREESPEC_ATTN_PERSISTENT=1 its
+// persistent form), kt the small-tree tcgen05 kernel (at most 32 nodes, keys on the
 // MMA's M side, key tiles cut evenly over the SMs). Measured on GB300 for a
 // 21-node tree over a 2048-key prefix (batch 8, 32 heads): mma.sync 58 us,
 // kt 81-84 us -- one CTA per SM exposes kt's startup, per-pair epilogues and
@@ -1415,12 +1415,17 @@ bool use_kt(int d, int n_max) {
     return e && strcmp(e, "kt") == 0;
 }
 
+bool use_tq(int d, int n_max) {
+    if (d != 128 || n_max > 128) return false;
+    const char *e = getenv("TREESPEC_ATTN_KERNEL");
+    if (e && *e) return strcmp(e, "tq") == 0;
+    return n_max > 32;
+}
+
 bool use_tc(int d, int n_max) {
     if (d != 128 || n_max > TcCfg::NODES) return false;
     const char *e = getenv("TREESPEC_ATTN_KERNEL");
-    if (e && strcmp(e, "mma") == 0) return false;
-    if (e && strcmp(e, "tc") == 0) return true;
-    return n_max > 32;
+    return e && strcmp(e, "tc") == 0;
 }
 
 Variant pick_variant(int d, int n_max) {
@@ -1458,6 +1463,13 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool 
         p.small_tree = true;
         p.kernel = "k_attn_kt";
         p.ws_bytes = attn_kt_ws_bytes(B, H);
+        return p;
+    }
+    if (use_tq(d, n_max)) {
+        p.tq = true;
+        p.n_pad = 128;
+        p.kernel = "k_attn_tq";
+        p.ws_bytes = 256;
         return p;
     }
     const Variant v = pick_variant(d, n_max);
@@ -1501,6 +1513,7 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
                              const PagedArgs &pg) {
     if (plan.small_tree)
         return launch_attn_kt(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, ws, status, s, why);
+    if (plan.tq) return launch_attn_tq(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, status, s, why, pg);
     const Variant v = pick_variant(d, t.n_max);
     CUtensorMap mk, mv;
     // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged

@@ -1,0 +1,495 @@
+// attn_tq.cu -- persistent tcgen05 tree attention with 128-key tiles, for trees
+// of up to 128 nodes and head_dim 128.
+//
+// What it computes: TreeAttention(u) = Attention(S_u) for every node u of the
+// token tree (SpecInfer, arXiv 2305.09781, Def. 4.1, Eq. 1-4): node i sees every
+// prefix key and the tree keys of its ancestors and itself (the topology-aware
+// causal mask of sec. 4.2, a bit test on the ancestor bitmask).
+//
+// GB300 design. Each CTA (one per SM) walks (request, head) items p = blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the K/V ring, the two score buffers and the
+// softmax run on across item boundaries.
+//   warp 0    TMA producer (lane 0): 128-key K and V tiles into a 3-stage ring
+//             (64 KB a stage), as 64-key boxes so that a paged cache (pages of
+//             64 keys) is read the same way
+//   warp 1    MMA issuer (lane 0): S = Q K^T (M = 128 node rows, N = 128 keys,
+//             K = 128 dims) with Q read from TMEM; O += P V (M = 128, N = 128
+//             dims, K = 128 keys) with P read from TMEM
+//   warps 2-9 softmax: the two warps of a TMEM lane quarter share its 32 node
+//             rows, one taking key columns 0-63 of the tile, the other 64-127;
+//             they exchange their half-row maxima through shared memory, so
+//             both apply the same running max; each writes its bf16 P over the
+//             first 32 columns of its own half of the score buffer, loads the
+//             next item's Q rows into the other Q buffer, and at the end of an
+//             item normalises and writes its half of each output row.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) (fp32 scores; P in bf16 pairs at
+// [x*128, x*128+32) and [x*128+64, x*128+96)), O [256,384), Q0 [384,448),
+// Q1 [448,512) (bf16 pairs). Every wait is bounded; on a timeout the CTA keeps
+// its barrier schedule, sets TS_STATUS_TIMEOUT and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "attn_common.cuh"
+#include "ts_internal.cuh"
+
+namespace ts {
+namespace {
+
+struct TqCfg {
+    static constexpr int D = 128, TKT = 128, HALF = 64, STAGES = 3, NODES = 128, SM_WARPS = 8;
+    static constexpr int THREADS = 64 + 32 * SM_WARPS;
+    static constexpr int BOX_BYTES = HALF * 128;          // one TMA box: 64 key rows x 128 bytes
+    static constexpr int OPB = TKT * 128;                 // a 64-dim half of a 128-key operand
+    static constexpr int TILE_BYTES = 2 * OPB;            // K (or V) of 128 keys x 128 dims
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
+    static constexpr int OFF_MX = STAGES * STAGE_BYTES;   // half-row maxima [2 parities][2 halves][128]
+    static constexpr int OFF_LS = OFF_MX + 2 * 2 * NODES * 4;   // half-row sums [2 halves][128]
+    static constexpr int REQ_CACHE = 1024;                // (n, P) of the first requests, in shared memory
+    static constexpr int OFF_REQ = OFF_LS + 2 * NODES * 4;
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1;
+    static constexpr int OFF_BAR = OFF_REQ + REQ_CACHE * 8;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512, S_COL = 0, O_COL = 256, Q_COL = 384;
+};
+
+struct TqItem {
+    int b, h, n, P, L, ntiles;
+};
+
+// Item p = b * H + h; (n, P) from the shared-memory copy when b is in it.
+__device__ __forceinline__ TqItem tq_item(const AttnArgs &a, const int2 *req, int p) {
+    TqItem it;
+    it.b = p / a.H;
+    it.h = p - it.b * a.H;
+    if (it.b < TqCfg::REQ_CACHE) {
+        const int2 r = req[it.b];
+        it.n = r.x;
+        it.P = r.y;
+    } else {
+        it.n = a.t.n_nodes[it.b];
+        it.P = a.prefix_len[it.b];
+    }
+    it.L = it.P + it.n;
+    const bool ok = it.n > 0 && it.n <= TqCfg::NODES && it.P >= 0 && it.L <= a.L_max;
+    it.ntiles = ok ? (it.L + TqCfg::TKT - 1) / TqCfg::TKT : 0;
+    return it;
+}
+
+// The next item after p (stride G) that has key tiles, or -1.
+__device__ __forceinline__ int tq_next(const AttnArgs &a, const int2 *req, int p, int G, int pairs) {
+    for (int q = p + G; q < pairs; q += G)
+        if (tq_item(a, req, q).ntiles > 0) return q;
+    return -1;
+}
+
+// Named barrier of the two softmax warps that share a TMEM lane quarter.
+__device__ __forceinline__ void pair_sync(int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
+}
+
+// The 128-byte half (dims hf*64 .. +64) of the Q row of DFS row `row` of an
+// item, given that row's node index r = perm[b][row] (null past n).
+__device__ __forceinline__ const uint4 *tq_q_src(const AttnArgs &a, const TqItem &it, int row, int r, int hf) {
+    if (row >= it.n || r < 0) return nullptr;
+    return (const uint4 *)(a.q + (((size_t)it.b * a.t.n_max + r) * a.H + it.h) * TqCfg::D + hf * 64);
+}
+
+// One softmax warp's half of an item's Q rows (rows quarter*32 + lane; zero
+// past n) into TMEM Q buffer qb.
+__device__ __forceinline__ void tq_load_q(const uint4 *src, uint32_t tmem, int quarter, int hf, int qb) {
+    uint32_t qw[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+        const uint4 v = src ? __ldg(src + c4) : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * c4] = v.x;
+        qw[4 * c4 + 1] = v.y;
+        qw[4 * c4 + 2] = v.z;
+        qw[4 * c4 + 3] = v.w;
+    }
+    tc_st32u(tmem + ((uint32_t)(quarter * 32) << 16) + TqCfg::Q_COL + qb * 64 + hf * 32, qw);
+    tc_wait_st();
+}
+
+__global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_constant__ CUtensorMap map_k,
+                                                               const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+    using C = TqCfg;
+    constexpr int D = C::D;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sm_base = smem_u32(sm);
+    volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout
+    float *mx_s = (float *)(sm + C::OFF_MX);
+    float *ls_s = (float *)(sm + C::OFF_LS);
+    int2 *req_s = (int2 *)(sm + C::OFF_REQ);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pairs = a.t.B * a.H, G = gridDim.x;
+    pdl_wait();
+    pdl_trigger();
+
+    const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
+    const uint32_t sfull = empty + 8 * C::STAGES, pfull = sfull + 16, pvdone = pfull + 16;
+    const uint32_t qready = pvdone + 16, ofree = qready + 16, fin = ofree + 8;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 32) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(sfull + 8 * x, 1);
+            mbar_init(pfull + 8 * x, C::SM_WARPS);
+            mbar_init(pvdone + 8 * x, 1);
+            mbar_init(qready + 8 * x, C::SM_WARPS);
+        }
+        mbar_init(ofree, C::SM_WARPS);
+        mbar_init(fin, 1);
+        misc[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // every role reads the requests' (n, P) at each item: one copy in shared memory
+    for (int b = tid; b < a.t.B && b < C::REQ_CACHE; b += C::THREADS) req_s[b] = make_int2(a.t.n_nodes[b], a.prefix_len[b]);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------------------------------------- TMA producer
+            int g = 0;
+            bool ok = true;
+            for (int p = blockIdx.x; p < pairs && ok; p += G) {
+                const TqItem it = tq_item(a, req_s, p);
+                if (it.ntiles == 0 && it.n > 0 && it.h == 0) flag(a.status, TS_STATUS_INDEX);
+                for (int j = 0; j < it.ntiles; ++j, ++g) {
+                    const int st = g % C::STAGES, key0 = j * C::TKT;
+                    const bool h1 = key0 + C::HALF < it.L;   // the tile's second 64 keys hold any key
+                    // rows (page ids) fetched before the wait
+                    const int row0 = tile_row(a, it.b, it.h, key0);
+                    const int row1 = h1 ? tile_row(a, it.b, it.h, key0 + C::HALF) : 0;
+                    if (g >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((g / C::STAGES) - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
+                    mbar_expect_tx(full + 8 * st, (h1 ? 2 : 1) * 4 * C::BOX_BYTES);
+                    for (int kh = 0; kh < (h1 ? 2 : 1); ++kh) {
+                        const int row = kh ? row1 : row0;
+#pragma unroll
+                        for (int dh = 0; dh < 2; ++dh) {
+                            tma_load_2d(kdst + dh * C::OPB + kh * C::BOX_BYTES, &map_k, dh * 64, row, full + 8 * st);
+                            tma_load_2d(vdst + dh * C::OPB + kh * C::BOX_BYTES, &map_v, dh * 64, row, full + 8 * st);
+                        }
+                    }
+                }
+            }
+            if (!ok) misc[1] = 1;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------------------------------------- MMA issuer
+            constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
+            bool ok = true;
+            // S of tile g into score buffer g & 1, A = Q buffer qb; the buffer's
+            // previous P (tile g - 2) must have been consumed by its PV
+            auto issue_s = [&](int g, int qb) -> bool {
+                const int st = g % C::STAGES, x = g & 1;
+                if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(g / C::STAGES) & 1u)) return false;
+                if (g >= 2 && !mbar_wait_bounded(pvdone + 8 * x, (uint32_t)((g - 2) >> 1) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::OPB + (kk & 3) * 32, 16, 1024);
+                    tc_mma_ts(tmem + C::S_COL + x * C::TKT, tmem + C::Q_COL + qb * 64 + kk * 8, bd, idesc_s, kk > 0);
+                }
+                tc_commit(sfull + 8 * x);
+                return true;
+            };
+            // O += P V for tile g; the first tile of item u (u >= 1) starts O afresh
+            // once item u - 1's output has been read out of it
+            auto issue_pv = [&](int g, bool first, int u) -> bool {
+                const int st = g % C::STAGES, x = g & 1;
+                if (first && u >= 1 && !mbar_wait_bounded(ofree, (uint32_t)(u - 1) & 1u)) return false;
+                if (!mbar_wait_bounded(pfull + 8 * x, (uint32_t)(g >> 1) & 1u)) return false;
+                tc_fence_after();
+                const uint32_t vbase = sm_base + st * C::STAGE_BYTES + C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < C::TKT / 16; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::OPB, 1024);
+                    tc_mma_ts(tmem + C::O_COL, tmem + C::S_COL + x * C::TKT + (kk >> 2) * 64 + (kk & 3) * 8, bd,
+                              idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(empty + 8 * st);
+                tc_commit(pvdone + 8 * x);
+                return true;
+            };
+            // S(g + 1) is issued before PV(g), also across item boundaries
+            int g = 0, u = 0, pend_g = -1, pend_u = 0;
+            bool pend_first = false;
+            for (int p = blockIdx.x; p < pairs && ok; p += G) {
+                const TqItem it = tq_item(a, req_s, p);
+                if (it.ntiles == 0) continue;
+                const int qb = u & 1;
+                if (!mbar_wait_bounded(qready + 8 * qb, (uint32_t)(u >> 1) & 1u)) { ok = false; break; }
+                tc_fence_after();
+                for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
+                    if (!issue_s(g, qb)) { ok = false; break; }
+                    if (pend_g >= 0 && !issue_pv(pend_g, pend_first, pend_u)) { ok = false; break; }
+                    pend_g = g;
+                    pend_first = j == 0;
+                    pend_u = u;
+                }
+                ++u;
+            }
+            if (ok && pend_g >= 0) ok = issue_pv(pend_g, pend_first, pend_u);
+            if (!ok) misc[1] = 1;
+            tc_commit(fin);   // completes once every MMA issued above has finished
+            if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
+        }
+        __syncwarp();
+    } else {   // ------------------------------------------------------ softmax
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;   // lane quarter; key half of the tile
+        const int row = quarter * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int n_max = a.t.n_max, W = TS_MASK_WORDS(n_max);
+        const float c = a.scale_log2;
+        bool ok = true;
+        int p = blockIdx.x;
+        while (p < pairs && tq_item(a, req_s, p).ntiles == 0) p += G;
+        int perm_cur = -1;   // perm[b][row] of the current item
+        if (p < pairs) {     // Q of the first item
+            const TqItem it = tq_item(a, req_s, p);
+            perm_cur = row < it.n ? a.t.perm[(size_t)it.b * n_max + row] : -1;
+            tq_load_q(tq_q_src(a, it, row, perm_cur, hf), tmem, quarter, hf, 0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qready);
+        }
+        int g = 0;
+        for (int u = 0; p < pairs; ++u) {
+            const TqItem it = tq_item(a, req_s, p);
+            const int nxt = tq_next(a, req_s, p, G, pairs);
+            const TqItem itn = nxt >= 0 ? tq_item(a, req_s, nxt) : it;
+            // the next item's perm entry now, an L2 prefetch of its Q row a tile
+            // later, the load itself two tiles after that: global latency off the
+            // softmax's path
+            const int perm_nxt = nxt >= 0 && row < itn.n ? a.t.perm[(size_t)itn.b * n_max + row] : -1;
+            const bool active = quarter * 32 < it.n;
+            uint32_t aw0 = 0u, aw1 = 0u, aw2 = 0u, aw3 = 0u;   // ancestor words of this row
+            if (row < it.n) {
+                const uint32_t *ar = a.t.anc + ((size_t)it.b * n_max + row) * W;
+                aw0 = ar[0];
+                if (W > 1) aw1 = ar[1];
+                if (W > 2) aw2 = ar[2];
+                if (W > 3) aw3 = ar[3];
+            }
+            float m_run = -INFINITY, l_run = 0.f;
+            const int jq = it.ntiles - 1 < 3 ? it.ntiles - 1 : 3;   // after this tile, the next item's Q
+            const int jp = jq < 1 ? jq : 1;                           // after this tile, its L2 prefetch
+            for (int j = 0; j < it.ntiles; ++j, ++g) {
+                const int x = g & 1;
+                if (ok && !mbar_wait_warp(sfull + 8 * x, (uint32_t)(g >> 1) & 1u)) ok = false;
+                tc_fence_after();
+                const int key_base = j * C::TKT, kh0 = key_base + hf * C::HALF;   // this warp's first key
+                const uint32_t ts_col = tl + C::S_COL + x * C::TKT + hf * C::HALF;
+                float sv[64];
+                float mh = -INFINITY;
+                if (ok && active) {
+                    tc_ld32(ts_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
+                    tc_ld32(ts_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+                    tc_wait_ld();
+                    if (kh0 + C::HALF > it.P) {   // tree keys or keys past the end in this half
+#pragma unroll
+                        for (int e = 0; e < C::HALF; ++e) {
+                            const int key = kh0 + e;
+                            bool vis = key < it.L;
+                            if (vis && key >= it.P) {
+                                const int tk = key - it.P;
+                                const uint32_t wd = tk < 32 ? aw0 : tk < 64 ? aw1 : tk < 96 ? aw2 : aw3;
+                                vis = (wd >> (tk & 31)) & 1u;
+                            }
+                            if (!vis) sv[e] = -INFINITY;
+                        }
+                    }
+                    float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+                    for (int e = 4; e < C::HALF; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+                    mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+                }
+                // the two halves' maxima: both warps of the quarter take the same row max
+                mx_s[((g & 1) * 2 + hf) * C::NODES + row] = mh;
+                pair_sync(quarter);
+                const float mo = mx_s[((g & 1) * 2 + (hf ^ 1)) * C::NODES + row];
+                if (ok && active) {
+                    const float mt = fmaxf(mh, mo);
+                    float alpha = 1.f;
+                    bool resc = false;
+                    if (m_run == -INFINITY) {
+                        m_run = mt;                          // nothing accumulated yet for this row
+                    } else if (mt > m_run + 8.f) {
+                        alpha = exp2f(m_run - mt);
+                        m_run = mt;
+                        resc = true;
+                    }
+                    if (__any_sync(0xffffffffu, resc)) {
+                        // the previous PV must have landed in O before O is rescaled
+                        const int gp = g - 1;
+                        if (j >= 1 && !mbar_wait_warp(pvdone + 8 * (gp & 1), (uint32_t)(gp >> 1) & 1u)) ok = false;
+                        tc_fence_after();
+                        if (ok) {
+#pragma unroll
+                            for (int q2 = 0; q2 < 2; ++q2) {
+                                float o[32];
+                                tc_ld32(tl + C::O_COL + hf * 64 + q2 * 32, o);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                                tc_st32(tl + C::O_COL + hf * 64 + q2 * 32, o);
+                            }
+                            tc_wait_st();
+                        }
+                        l_run *= alpha;
+                    }
+                    if (ok) {
+                        const float mu = m_run == -INFINITY ? 0.f : m_run;
+                        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int e = 0; e < C::HALF; e += 2) {
+                            float r0, r1;
+                            pk[e >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[e], c, -mu)), exp2f(__fmaf_rn(sv[e + 1], c, -mu)),
+                                                   r0, r1);
+                            ls[(e >> 1) & 3] += r0 + r1;
+                        }
+                        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                        tc_st32u(ts_col, pk);   // P over the first 32 columns of this half
+                        tc_wait_st();
+                    }
+                }
+                if (key_base + C::TKT > it.L) {
+                    // last tile of the item: zero the V rows past its keys (they may
+                    // hold anything, even NaN, or stale rows of an earlier tile)
+                    const int st = g % C::STAGES;
+                    if (ok && !mbar_wait_warp(full + 8 * st, (uint32_t)(g / C::STAGES) & 1u)) ok = false;
+                    unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
+                    const int r0 = it.L - key_base;
+                    for (int idx = tid - 64; ok && idx < (C::TKT - r0) * 16; idx += 32 * C::SM_WARPS) {
+                        const int r = r0 + (idx >> 4), c16 = idx & 15;
+                        *(uint4 *)(vt + (c16 >> 3) * C::OPB + r * 128 + ((c16 & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pfull + 8 * x);
+                if (j == jp && nxt >= 0) {
+                    const uint4 *qs = tq_q_src(a, itn, row, perm_nxt, hf);
+                    if (qs) asm volatile("prefetch.global.L2 [%0];" ::"l"(qs));
+                }
+                if (j == jq && nxt >= 0) {
+                    // the next item's Q rows into the other Q buffer: every S of the
+                    // item that used it finished before this item's first S
+                    if (ok) tq_load_q(tq_q_src(a, itn, row, perm_nxt, hf), tmem, quarter, hf, (u + 1) & 1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(qready + 8 * ((u + 1) & 1));
+                }
+            }
+            // ---- epilogue: O holds the item once its last PV has finished
+            const int gl = g - 1;
+            if (ok && !mbar_wait_warp(pvdone + 8 * (gl & 1), (uint32_t)(gl >> 1) & 1u)) ok = false;
+            tc_fence_after();
+            ls_s[hf * C::NODES + row] = l_run;
+            pair_sync(quarter);
+            const float lsum = ls_s[row] + ls_s[C::NODES + row];
+            if (ok && active) {
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                uint4 *dst = nullptr;
+                if (row < it.n && perm_cur >= 0)
+                    dst = (uint4 *)(a.out + (((size_t)it.b * n_max + perm_cur) * a.H + it.h) * D + hf * 64);
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float o[32];
+                    tc_ld32(tl + C::O_COL + hf * 64 + q2 * 32, o);
+                    tc_wait_ld();
+                    if (dst) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            float d0, d1;
+                            uint4 v;
+                            v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
+                            v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
+                            v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
+                            v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
+                            dst[q2 * 4 + c8] = v;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ofree);   // O may be overwritten by the next item now
+            p = nxt < 0 ? pairs : nxt;
+            perm_cur = perm_nxt;
+        }
+        if (!ok) misc[1] = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    if (misc[1] && tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
+                           uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg) {
+    CUtensorMap mk, mv;
+    // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
+    const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
+    if (!make_map(&mk, k_cache, TqCfg::D, rows, TqCfg::HALF) || !make_map(&mv, v_cache, TqCfg::D, rows, TqCfg::HALF)) {
+        *why = "cuTensorMapEncodeTiled failed for the KV cache";
+        return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tq, cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    AttnArgs a;
+    a.out = (__nv_bfloat16 *)out;
+    a.q = (const __nv_bfloat16 *)q;
+    a.prefix_len = prefix_len;
+    a.t = t;
+    a.H = H;
+    a.L_max = L_max;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.chunk_tiles = 0;
+    a.splits = 1;
+    a.n_pad = TqCfg::NODES;
+    a.counters = nullptr;
+    a.part_ml = nullptr;
+    a.part_o = nullptr;
+    a.status = status;
+    a.bt = pg.bt;
+    a.max_pages = pg.max_pages;
+    a.num_pages = pg.num_pages;
+    const int pairs = t.B * H;
+    const int grid = pairs < num_sms() ? pairs : num_sms();
+    if (grid < 1) return cudaSuccess;
+    return launch(k_attn_tq, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
+}
+
+}  // namespace ts

@@ -101,6 +101,7 @@ struct AttnPlan {
     bool persistent;   // the persistent tcgen05 kernel walks the (b, h) items
     bool small_tree;   // the small-tree tcgen05 kernel (key tiles cut evenly over the SMs)
     const char *kernel;  // name of the kernel the launch uses
+    bool tq = false;     // the persistent 128-key-tile tcgen05 kernel
 };
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool allow_small_tree = true);
 
@@ -113,6 +114,10 @@ size_t attn_kt_ws_bytes(int B, int H);
 cudaError_t launch_attn_kt(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale, void *ws,
                            uint32_t *status, cudaStream_t s, const char **why);
+// Persistent tcgen05 kernel with 128-key tiles (head_dim 128, at most 128 nodes).
+cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
+                           uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg);
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,
