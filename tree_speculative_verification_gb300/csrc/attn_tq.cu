@@ -86,6 +86,30 @@ __device__ __forceinline__ int tq_next(const AttnArgs &a, const int2 *req, int p
     return -1;
 }
 
+// A 32-bit global load issued here (the asm is not moved), its result waited
+// for only where it is first used.
+__device__ __forceinline__ int ld_early(const int32_t *p) {
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Ancestor words (up to four) of node row `row` of an item, loaded early; zero past n.
+struct TqAnc {
+    uint32_t w0, w1, w2, w3;
+};
+__device__ __forceinline__ TqAnc tq_anc(const AttnArgs &a, const TqItem &it, int row, bool any) {
+    TqAnc r{0u, 0u, 0u, 0u};
+    if (!any || row >= it.n) return r;
+    const int W = TS_MASK_WORDS(a.t.n_max);
+    const int32_t *ar = (const int32_t *)a.t.anc + ((size_t)it.b * a.t.n_max + row) * W;
+    r.w0 = (uint32_t)ld_early(ar);
+    if (W > 1) r.w1 = (uint32_t)ld_early(ar + 1);
+    if (W > 2) r.w2 = (uint32_t)ld_early(ar + 2);
+    if (W > 3) r.w3 = (uint32_t)ld_early(ar + 3);
+    return r;
+}
+
 // Named barrier of the two softmax warps that share a TMEM lane quarter.
 __device__ __forceinline__ void pair_sync(int quarter) {
     asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
@@ -263,15 +287,17 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
         const int quarter = warp & 3, hf = (warp - 2) >> 2;   // lane quarter; key half of the tile
         const int row = quarter * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int n_max = a.t.n_max, W = TS_MASK_WORDS(n_max);
+        const int n_max = a.t.n_max;
         const float c = a.scale_log2;
         bool ok = true;
         int p = blockIdx.x;
         while (p < pairs && tq_item(a, req_s, p).ntiles == 0) p += G;
         int perm_cur = -1;   // perm[b][row] of the current item
+        TqAnc anc_cur{0u, 0u, 0u, 0u};   // its ancestor words of this row
         if (p < pairs) {     // Q of the first item
             const TqItem it = tq_item(a, req_s, p);
             perm_cur = row < it.n ? a.t.perm[(size_t)it.b * n_max + row] : -1;
+            anc_cur = tq_anc(a, it, row, true);
             tq_load_q(tq_q_src(a, it, row, perm_cur, hf), tmem, quarter, hf, 0);
             tc_fence_before();
             __syncwarp();
@@ -282,19 +308,13 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             const TqItem it = tq_item(a, req_s, p);
             const int nxt = tq_next(a, req_s, p, G, pairs);
             const TqItem itn = nxt >= 0 ? tq_item(a, req_s, nxt) : it;
-            // the next item's perm entry now, an L2 prefetch of its Q row a tile
-            // later, the load itself two tiles after that: global latency off the
-            // softmax's path
-            const int perm_nxt = nxt >= 0 && row < itn.n ? a.t.perm[(size_t)itn.b * n_max + row] : -1;
+            // the next item's perm entry and ancestor words issued now (used an
+            // item later), an L2 prefetch of its Q row a tile later, the Q load
+            // itself two tiles after that: global latency off the softmax's path
+            const int perm_nxt = nxt >= 0 && row < itn.n ? ld_early(a.t.perm + (size_t)itn.b * n_max + row) : -1;
+            const TqAnc anc_nxt = tq_anc(a, itn, row, nxt >= 0);
             const bool active = quarter * 32 < it.n;
-            uint32_t aw0 = 0u, aw1 = 0u, aw2 = 0u, aw3 = 0u;   // ancestor words of this row
-            if (row < it.n) {
-                const uint32_t *ar = a.t.anc + ((size_t)it.b * n_max + row) * W;
-                aw0 = ar[0];
-                if (W > 1) aw1 = ar[1];
-                if (W > 2) aw2 = ar[2];
-                if (W > 3) aw3 = ar[3];
-            }
+            const uint32_t aw0 = anc_cur.w0, aw1 = anc_cur.w1, aw2 = anc_cur.w2, aw3 = anc_cur.w3;
             float m_run = -INFINITY, l_run = 0.f;
             const int jq = it.ntiles - 1 < 3 ? it.ntiles - 1 : 3;   // after this tile, the next item's Q
             const int jp = jq < 1 ? jq : 1;                           // after this tile, its L2 prefetch
@@ -311,17 +331,25 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                     tc_ld32(ts_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
                     tc_wait_ld();
                     if (kh0 + C::HALF > it.P) {   // tree keys or keys past the end in this half
-#pragma unroll
-                        for (int e = 0; e < C::HALF; ++e) {
-                            const int key = kh0 + e;
-                            bool vis = key < it.L;
-                            if (vis && key >= it.P) {
-                                const int tk = key - it.P;
-                                const uint32_t wd = tk < 32 ? aw0 : tk < 64 ? aw1 : tk < 96 ? aw2 : aw3;
-                                vis = (wd >> (tk & 31)) & 1u;
-                            }
-                            if (!vis) sv[e] = -INFINITY;
+                        // visibility of keys kh0 .. kh0+63 as one 64-bit window: prefix
+                        // keys visible, tree key t visible iff ancestor bit t, none
+                        // from L on
+                        const unsigned long long lo = (unsigned long long)aw0 | ((unsigned long long)aw1 << 32);
+                        const unsigned long long hi = (unsigned long long)aw2 | ((unsigned long long)aw3 << 32);
+                        const int t0 = kh0 - it.P;   // tree index of the first key, > -64
+                        unsigned long long win;
+                        if (t0 >= 0) {
+                            win = t0 >= 64 ? (t0 >= 128 ? 0ull : hi >> (t0 - 64))
+                                           : (t0 == 0 ? lo : (lo >> t0) | (hi << (64 - t0)));
+                        } else {
+                            win = (lo << (-t0)) | ((1ull << (-t0)) - 1ull);
                         }
+                        const int valid = it.L - kh0;   // keys of this half before L
+                        if (valid < 64) win &= valid <= 0 ? 0ull : (1ull << valid) - 1ull;
+                        const uint32_t wl = (uint32_t)win, wh = (uint32_t)(win >> 32);
+#pragma unroll
+                        for (int e = 0; e < C::HALF; ++e)
+                            if (!(((e < 32 ? wl : wh) >> (e & 31)) & 1u)) sv[e] = -INFINITY;
                     }
                     float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
@@ -443,6 +471,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             if (lane == 0) mbar_arrive(ofree);   // O may be overwritten by the next item now
             p = nxt < 0 ? pairs : nxt;
             perm_cur = perm_nxt;
+            anc_cur = anc_nxt;
         }
         if (!ok) misc[1] = 1;
     }
