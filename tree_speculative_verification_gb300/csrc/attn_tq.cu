@@ -45,10 +45,12 @@ struct TqCfg {
     static constexpr int OPB = TKT * 128;                 // a 64-dim half of a 128-key operand
     static constexpr int TILE_BYTES = 2 * OPB;            // K (or V) of 128 keys x 128 dims
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
-    static constexpr int OFF_MX = STAGES * STAGE_BYTES;   // half-row maxima [2 parities][2 halves][128]
-    static constexpr int OFF_LS = OFF_MX + 2 * 2 * NODES * 4;   // half-row sums [2 halves][128]
-    static constexpr int REQ_CACHE = 1024;                // (n, P) of the first requests, in shared memory
-    static constexpr int OFF_REQ = OFF_LS + 2 * NODES * 4;
+    static constexpr int OFF_MX = STAGES * STAGE_BYTES;   // partial row maxima [2 parities][4 slots][128]
+    static constexpr int OFF_LS = OFF_MX + 2 * 4 * NODES * 4;   // partial row sums [4 slots][128]
+    static constexpr int XO_STRIDE = 33;                  // padded row of the O exchange
+    static constexpr int OFF_XO = OFF_LS + 4 * NODES * 4; // upper-copy O chunks [2 quarters][2 halves][32][33]
+    static constexpr int REQ_CACHE = 512;                 // (n, P) of the first requests, in shared memory
+    static constexpr int OFF_REQ = OFF_XO + 4 * 32 * XO_STRIDE * 4;
     static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1;
     static constexpr int OFF_BAR = OFF_REQ + REQ_CACHE * 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -115,6 +117,29 @@ __device__ __forceinline__ void pair_sync(int quarter) {
     asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
 }
 
+// Named barrier of the four softmax warps of lane quarters lq and lq + 2 (the
+// two copies of node rows lq*32 .. +32 when rows are duplicated).
+__device__ __forceinline__ void group_sync(int lq) {
+    asm volatile("bar.sync %0, 128;" ::"r"(6 + lq) : "memory");
+}
+
+// Visibility of the keys k0 .. k0 + 63 of an item for one node row, bit e for
+// key k0 + e: prefix keys visible, tree key t visible iff ancestor bit t (lo:
+// bits 0-63, hi: 64-127), nothing from L on. Needs k0 + 64 > P.
+__device__ __forceinline__ unsigned long long tq_window(unsigned long long lo, unsigned long long hi, int k0, int P,
+                                                        int L) {
+    const int t0 = k0 - P;   // tree index of the first key, > -64
+    unsigned long long win;
+    if (t0 >= 0) {
+        win = t0 >= 64 ? (t0 >= 128 ? 0ull : hi >> (t0 - 64)) : (t0 == 0 ? lo : (lo >> t0) | (hi << (64 - t0)));
+    } else {
+        win = (lo << (-t0)) | ((1ull << (-t0)) - 1ull);
+    }
+    const int valid = L - k0;   // keys before L
+    if (valid < 64) win &= valid <= 0 ? 0ull : (1ull << valid) - 1ull;
+    return win;
+}
+
 // The 128-byte half (dims hf*64 .. +64) of the Q row of DFS row `row` of an
 // item, given that row's node index r = perm[b][row] (null past n).
 __device__ __forceinline__ const uint4 *tq_q_src(const AttnArgs &a, const TqItem &it, int row, int r, int hf) {
@@ -138,6 +163,9 @@ __device__ __forceinline__ void tq_load_q(const uint4 *src, uint32_t tmem, int q
     tc_wait_st();
 }
 
+// DUP: every tree of the launch has at most 64 nodes, and TMEM lanes 64-127
+// hold a second copy of rows 0-63 (see the file comment).
+template <bool DUP>
 __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_constant__ CUtensorMap map_k,
                                                                const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
     using C = TqCfg;
@@ -252,8 +280,11 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
 #pragma unroll
                 for (int kk = 0; kk < C::TKT / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::OPB, 1024);
-                    tc_mma_ts(tmem + C::O_COL, tmem + C::S_COL + x * C::TKT + (kk >> 2) * 64 + (kk & 3) * 8, bd,
-                              idesc_pv, (!first || kk > 0) ? 1u : 0u);
+                    // P of keys 16kk .. +16: at 64-key halves (cols 0-31, 64-95), or with
+                    // duplicated rows at 32-key blocks (cols 0-15, 32-47, 64-79, 96-111)
+                    const uint32_t pc = DUP ? (kk >> 1) * 32 + (kk & 1) * 8 : (kk >> 2) * 64 + (kk & 3) * 8;
+                    tc_mma_ts(tmem + C::O_COL, tmem + C::S_COL + x * C::TKT + pc, bd, idesc_pv,
+                              (!first || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(empty + 8 * st);
                 tc_commit(pvdone + 8 * x);
@@ -284,11 +315,19 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
         }
         __syncwarp();
     } else {   // ------------------------------------------------------ softmax
-        const int quarter = warp & 3, hf = (warp - 2) >> 2;   // lane quarter; key half of the tile
-        const int row = quarter * 32 + lane;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
+        const int prow = quarter * 32 + lane;                  // this lane's TMEM row
+        const int row = DUP ? (prow & 63) : prow;              // its node row
+        const bool upper = DUP && quarter >= 2;                // the second copy of the row
         const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
         const int n_max = a.t.n_max;
         const float c = a.scale_log2;
+        // 32-key blocks of a tile this warp scores (two, or one with duplicated
+        // rows) and, with duplicated rows, the block whose P it zeroes
+        constexpr int NKB = DUP ? 1 : 2;
+        const int kb0 = DUP ? 2 * (quarter >> 1) + hf : 2 * hf;
+        const int kbz = quarter >= 2 ? hf : 2 + hf;
+        float *xo = (float *)(sm + C::OFF_XO) + ((quarter & 1) * 2 + hf) * 32 * C::XO_STRIDE + lane * C::XO_STRIDE;
         bool ok = true;
         int p = blockIdx.x;
         while (p < pairs && tq_item(a, req_s, p).ntiles == 0) p += G;
@@ -313,8 +352,9 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             // itself two tiles after that: global latency off the softmax's path
             const int perm_nxt = nxt >= 0 && row < itn.n ? ld_early(a.t.perm + (size_t)itn.b * n_max + row) : -1;
             const TqAnc anc_nxt = tq_anc(a, itn, row, nxt >= 0);
-            const bool active = quarter * 32 < it.n;
-            const uint32_t aw0 = anc_cur.w0, aw1 = anc_cur.w1, aw2 = anc_cur.w2, aw3 = anc_cur.w3;
+            const bool active = (row & ~31) < it.n;
+            const unsigned long long anc_lo = (unsigned long long)anc_cur.w0 | ((unsigned long long)anc_cur.w1 << 32);
+            const unsigned long long anc_hi = (unsigned long long)anc_cur.w2 | ((unsigned long long)anc_cur.w3 << 32);
             float m_run = -INFINITY, l_run = 0.f;
             const int jq = it.ntiles - 1 < 3 ? it.ntiles - 1 : 3;   // after this tile, the next item's Q
             const int jp = jq < 1 ? jq : 1;                           // after this tile, its L2 prefetch
@@ -322,44 +362,38 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                 const int x = g & 1;
                 if (ok && !mbar_wait_warp(sfull + 8 * x, (uint32_t)(g >> 1) & 1u)) ok = false;
                 tc_fence_after();
-                const int key_base = j * C::TKT, kh0 = key_base + hf * C::HALF;   // this warp's first key
-                const uint32_t ts_col = tl + C::S_COL + x * C::TKT + hf * C::HALF;
-                float sv[64];
+                const int key_base = j * C::TKT, k0 = key_base + kb0 * 32;   // this warp's first key
+                const uint32_t sb = tl + C::S_COL + x * C::TKT;
+                float sv[32 * NKB];
                 float mh = -INFINITY;
                 if (ok && active) {
-                    tc_ld32(ts_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
-                    tc_ld32(ts_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+                    tc_ld32(sb + kb0 * 32, *reinterpret_cast<float(*)[32]>(&sv[0]));
+                    if constexpr (NKB == 2) tc_ld32(sb + (kb0 + 1) * 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
                     tc_wait_ld();
-                    if (kh0 + C::HALF > it.P) {   // tree keys or keys past the end in this half
-                        // visibility of keys kh0 .. kh0+63 as one 64-bit window: prefix
-                        // keys visible, tree key t visible iff ancestor bit t, none
-                        // from L on
-                        const unsigned long long lo = (unsigned long long)aw0 | ((unsigned long long)aw1 << 32);
-                        const unsigned long long hi = (unsigned long long)aw2 | ((unsigned long long)aw3 << 32);
-                        const int t0 = kh0 - it.P;   // tree index of the first key, > -64
-                        unsigned long long win;
-                        if (t0 >= 0) {
-                            win = t0 >= 64 ? (t0 >= 128 ? 0ull : hi >> (t0 - 64))
-                                           : (t0 == 0 ? lo : (lo >> t0) | (hi << (64 - t0)));
-                        } else {
-                            win = (lo << (-t0)) | ((1ull << (-t0)) - 1ull);
-                        }
-                        const int valid = it.L - kh0;   // keys of this half before L
-                        if (valid < 64) win &= valid <= 0 ? 0ull : (1ull << valid) - 1ull;
+                    if (k0 + 32 * NKB > it.P) {   // tree keys or keys past the end in these blocks
+                        const unsigned long long win = tq_window(anc_lo, anc_hi, k0, it.P, it.L);
                         const uint32_t wl = (uint32_t)win, wh = (uint32_t)(win >> 32);
 #pragma unroll
-                        for (int e = 0; e < C::HALF; ++e)
+                        for (int e = 0; e < 32 * NKB; ++e)
                             if (!(((e < 32 ? wl : wh) >> (e & 31)) & 1u)) sv[e] = -INFINITY;
                     }
                     float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-                    for (int e = 4; e < C::HALF; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
+                    for (int e = 4; e < 32 * NKB; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
                     mh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
                 }
-                // the two halves' maxima: both warps of the quarter take the same row max
-                mx_s[((g & 1) * 2 + hf) * C::NODES + row] = mh;
-                pair_sync(quarter);
-                const float mo = mx_s[((g & 1) * 2 + (hf ^ 1)) * C::NODES + row];
+                // the partial maxima of the row's warps: all take the same row max
+                float mo;
+                if constexpr (DUP) {
+                    mx_s[((g & 1) * 4 + kb0) * C::NODES + row] = mh;
+                    group_sync(quarter & 1);
+                    mo = fmaxf(fmaxf(mx_s[((g & 1) * 4) * C::NODES + row], mx_s[((g & 1) * 4 + 1) * C::NODES + row]),
+                               fmaxf(mx_s[((g & 1) * 4 + 2) * C::NODES + row], mx_s[((g & 1) * 4 + 3) * C::NODES + row]));
+                } else {
+                    mx_s[((g & 1) * 4 + hf) * C::NODES + row] = mh;
+                    pair_sync(quarter);
+                    mo = mx_s[((g & 1) * 4 + (hf ^ 1)) * C::NODES + row];
+                }
                 if (ok && active) {
                     const float mt = fmaxf(mh, mo);
                     float alpha = 1.f;
@@ -393,16 +427,26 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                     if (ok) {
                         const float mu = m_run == -INFINITY ? 0.f : m_run;
                         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                        uint32_t pk[32];
+                        uint32_t pk[16 * NKB];
 #pragma unroll
-                        for (int e = 0; e < C::HALF; e += 2) {
+                        for (int e = 0; e < 32 * NKB; e += 2) {
                             float r0, r1;
                             pk[e >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[e], c, -mu)), exp2f(__fmaf_rn(sv[e + 1], c, -mu)),
                                                    r0, r1);
                             ls[(e >> 1) & 3] += r0 + r1;
                         }
                         l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                        tc_st32u(ts_col, pk);   // P over the first 32 columns of this half
+                        if constexpr (DUP) {
+                            // P over the first 16 columns of the scored block; this copy of
+                            // the row takes no part in the other copy's keys
+                            tc_st16u(sb + kb0 * 32, pk);
+                            uint32_t zr[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) zr[e] = 0u;
+                            tc_st16u(sb + kbz * 32, zr);
+                        } else {
+                            tc_st32u(sb + hf * 64, pk);   // P over the first 32 columns of this half
+                        }
                         tc_wait_st();
                     }
                 }
@@ -439,30 +483,52 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             const int gl = g - 1;
             if (ok && !mbar_wait_warp(pvdone + 8 * (gl & 1), (uint32_t)(gl >> 1) & 1u)) ok = false;
             tc_fence_after();
-            ls_s[hf * C::NODES + row] = l_run;
-            pair_sync(quarter);
-            const float lsum = ls_s[row] + ls_s[C::NODES + row];
-            if (ok && active) {
-                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                uint4 *dst = nullptr;
-                if (row < it.n && perm_cur >= 0)
-                    dst = (uint4 *)(a.out + (((size_t)it.b * n_max + perm_cur) * a.H + it.h) * D + hf * 64);
+            float lsum;
+            if constexpr (DUP) {
+                ls_s[kb0 * C::NODES + row] = l_run;
+                group_sync(quarter & 1);
+                lsum = (ls_s[row] + ls_s[C::NODES + row]) + (ls_s[2 * C::NODES + row] + ls_s[3 * C::NODES + row]);
+            } else {
+                ls_s[hf * C::NODES + row] = l_run;
+                pair_sync(quarter);
+                lsum = ls_s[row] + ls_s[C::NODES + row];
+            }
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            uint4 *dst = nullptr;
+            if (ok && active && !upper && row < it.n && perm_cur >= 0)
+                dst = (uint4 *)(a.out + (((size_t)it.b * n_max + perm_cur) * a.H + it.h) * D + hf * 64);
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    float o[32];
+            for (int q2 = 0; q2 < 2; ++q2) {   // 32 dims at a time
+                float o[32];
+                if (ok && active) {
                     tc_ld32(tl + C::O_COL + hf * 64 + q2 * 32, o);
                     tc_wait_ld();
-                    if (dst) {
+                } else {
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            float d0, d1;
-                            uint4 v;
-                            v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
-                            v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
-                            v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
-                            v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
-                            dst[q2 * 4 + c8] = v;
-                        }
+                    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+                }
+                if constexpr (DUP) {   // the upper copy's partial row goes to its lower twin
+                    if (upper) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) xo[e] = o[e];
+                    }
+                    group_sync(quarter & 1);
+                    if (!upper) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] += xo[e];
+                    }
+                    group_sync(quarter & 1);
+                }
+                if (dst) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float d0, d1;
+                        uint4 v;
+                        v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
+                        v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
+                        v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
+                        v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
+                        dst[q2 * 4 + c8] = v;
                     }
                 }
             }
@@ -495,7 +561,9 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_attn_tq, cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
+    const bool dup = t.n_max <= 64;
+    cudaError_t e = cudaFuncSetAttribute(dup ? k_attn_tq<true> : k_attn_tq<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
     if (e != cudaSuccess) return e;
     AttnArgs a;
     a.out = (__nv_bfloat16 *)out;
@@ -518,7 +586,8 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     const int pairs = t.B * H;
     const int grid = pairs < num_sms() ? pairs : num_sms();
     if (grid < 1) return cudaSuccess;
-    return launch(k_attn_tq, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
+    if (dup) return launch(k_attn_tq<true>, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
+    return launch(k_attn_tq<false>, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
 }
 
 }  // namespace ts
