@@ -124,4 +124,10 @@ class DeviceStep:
 
     def launches_per_step(self, kind: str | None = None) -> int:
         kind = kind or self.w.verify
-        return 1 + (3 if self.attention else 0) + (2 if kind == "both" else 1)
+        attn = 0
+        if self.attention:   # "a+b" names an attention call of two launches
+            w = self.w
+            name = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max,
+                                        api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
+            attn = 2 + len(name.split("+"))
+        return 1 + attn + (2 if kind == "both" else 1)
