@@ -55,6 +55,7 @@ class DeviceStep:
         self.mss_count = torch.zeros(B, dtype=torch.int32, device=dev)
         self.argmax = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
         self.ws_greedy = api.workspace(api.TS_OP_VERIFY_GREEDY, B, n_max=n_max, V=w.V, device=dev)
+        self._side = None   # verification stream, created on first use
         self.attention = attention and w.q is not None
         if self.attention:
             bf = w.dtype == "bf16"
@@ -108,13 +109,25 @@ class DeviceStep:
                       self.status, stream)
 
     def run(self, kind: str | None = None, stream=None):
-        self.build(stream)
-        if self.attention:
-            self.append(stream)
-            self.attend(stream)
-        self.verify(kind, stream)
-        if self.attention:
-            self.commit(kind, stream)
+        """One step. Verification reads only the tree and the logits, so it runs on
+        a second stream beside the KV append and the attention; the commit, which
+        needs the accepted path and the appended rows, waits for both."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.build(main)
+        if not self.attention:
+            self.verify(kind, main)
+            return
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.device)
+            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        self._fork.record(main)
+        self._side.wait_event(self._fork)
+        self.verify(kind, self._side)
+        self._join.record(self._side)
+        self.append(main)
+        self.attend(main)
+        main.wait_event(self._join)
+        self.commit(kind, main)
 
     def accepted(self, kind: str | None = None) -> int:
         """Tokens the last verification produced, over all requests."""
