@@ -119,3 +119,28 @@ def test_binding_fails_loudly_without_library(tmp_path):
             api.load_library(str(tmp_path / "missing.so"))
     finally:
         api._lib = saved
+
+
+@pytest.mark.parametrize("n_max,d,expect", [
+    (21, 128, "k_attn_bf16<"),      # the LLaMA-7B-shaped expansion tree: mma.sync
+    (32, 128, "k_attn_bf16<"),
+    (33, 128, "k_attn_tq"),         # 33..128 nodes: persistent tcgen05, 128-key tiles
+    (47, 128, "k_attn_tq"),
+    (128, 128, "k_attn_tq"),
+    (129, 128, "k_attn_bf16<"),
+    (47, 64, "k_attn_bf16<"),       # head_dim 64: mma.sync only
+])
+def test_kernel_choice(lib, n_max, d, expect, monkeypatch):
+    """attn_plan's default choice is host logic: the same without a GPU."""
+    for var in ("TREESPEC_ATTN_KERNEL", "TREESPEC_ATTN_SPLITS", "TREESPEC_ATTN_PERSISTENT"):
+        monkeypatch.delenv(var, raising=False)
+    name = api.attention_kernel(8, 32, n_max, d, 2048 + n_max, api.TS_BF16)
+    assert name.startswith(expect), name
+    assert api.attention_kernel(8, 32, n_max, d, 2048 + n_max, api.TS_F32) == "k_attn_f32"
+
+
+@pytest.mark.parametrize("force,n_max,expect", [("mma", 47, "k_attn_bf16<"), ("tc", 47, "k_attn_tc"),
+                                                 ("tq", 21, "k_attn_tq"), ("kt", 21, "k_attn_kt")])
+def test_kernel_override(lib, force, n_max, expect, monkeypatch):
+    monkeypatch.setenv("TREESPEC_ATTN_KERNEL", force)
+    assert api.attention_kernel(8, 32, n_max, 128, 2048 + n_max, api.TS_BF16).startswith(expect)
