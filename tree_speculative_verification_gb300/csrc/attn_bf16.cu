@@ -403,21 +403,20 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
                     }
                 }
             }
-            // P^T (bf16) in the B-operand layout; p = exp2(s * c - m)
+            // P^T (bf16) in the B-operand layout; p = exp2(s * c - m); the row sums
+            // take the fp32 probabilities, O their bf16 roundings
             uint32_t pb[NT][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const float mu0 = m_run[j][0] == -INFINITY ? 0.f : m_run[j][0];
                 const float mu1 = m_run[j][1] == -INFINITY ? 0.f : m_run[j][1];
-                float r0, r1, r2, r3;
-                const uint32_t x0 = pack_bf16(exp2f(__fmaf_rn(sacc[j][0], c, -mu0)),
-                                              exp2f(__fmaf_rn(sacc[j][1], c, -mu1)), r0, r1);
-                const uint32_t x1 = pack_bf16(exp2f(__fmaf_rn(sacc[j][2], c, -mu0)),
-                                              exp2f(__fmaf_rn(sacc[j][3], c, -mu1)), r2, r3);
-                l_run[j][0] += r0 + r2;
-                l_run[j][1] += r1 + r3;
-                pb[j][0] = movm_t(x0);
-                pb[j][1] = movm_t(x1);
+                const float p0 = exp2f(__fmaf_rn(sacc[j][0], c, -mu0)), p1 = exp2f(__fmaf_rn(sacc[j][1], c, -mu1));
+                const float p2 = exp2f(__fmaf_rn(sacc[j][2], c, -mu0)), p3 = exp2f(__fmaf_rn(sacc[j][3], c, -mu1));
+                const __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1), b23 = __floats2bfloat162_rn(p2, p3);
+                l_run[j][0] += p0 + p2;
+                l_run[j][1] += p1 + p3;
+                pb[j][0] = movm_t(*reinterpret_cast<const uint32_t *>(&b01));
+                pb[j][1] = movm_t(*reinterpret_cast<const uint32_t *>(&b23));
             }
             // O^T += V^T P^T
 #pragma unroll
