@@ -15,17 +15,25 @@
 //   warp 1    MMA issuer (lane 0): S = Q K^T (M = 128 node rows, N = 128 keys,
 //             K = 128 dims) with Q read from TMEM; O += P V (M = 128, N = 128
 //             dims, K = 128 keys) with P read from TMEM
-//   warps 2-9 softmax: the two warps of a TMEM lane quarter share its 32 node
-//             rows, one taking key columns 0-63 of the tile, the other 64-127;
-//             they exchange their half-row maxima through shared memory, so
-//             both apply the same running max; each writes its bf16 P over the
-//             first 32 columns of its own half of the score buffer, loads the
+//   warps 2-9 softmax. A warp reaches only its own TMEM lane quarter. Trees
+//             of more than 64 nodes (DUP = false): the two warps of a quarter
+//             share its 32 node rows, one taking key columns 0-63 of the tile,
+//             the other 64-127. Trees of up to 64 nodes (DUP = true): lanes
+//             64-127 hold a second copy of Q's rows 0-63, so all four quarters
+//             (all four SM sub-partitions) work; the four warps of a node row
+//             take 32 keys each, each copy of the row gets zero P for the 64
+//             keys the other copy takes, and O's rows r and r + 64 are two
+//             partial sums the epilogue adds through shared memory. The warps
+//             of a row exchange their partial maxima (and at the end their
+//             sums) through shared memory, so all apply the same running max;
+//             each writes its bf16 P over the scores it came from, loads the
 //             next item's Q rows into the other Q buffer, and at the end of an
-//             item normalises and writes its half of each output row.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) (fp32 scores; P in bf16 pairs at
-// [x*128, x*128+32) and [x*128+64, x*128+96)), O [256,384), Q0 [384,448),
-// Q1 [448,512) (bf16 pairs). Every wait is bounded; on a timeout the CTA keeps
-// its barrier schedule, sets TS_STATUS_TIMEOUT and frees its TMEM.
+//             item normalises and writes its part of each output row.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) (fp32 scores; P in bf16 pairs:
+// keys 0-63 at [x*128, +32) and 64-127 at [x*128+64, +32), or with DUP key block
+// kb (32 keys) at [x*128 + kb*32, +16)), O [256,384), Q0 [384,448), Q1 [448,512)
+// (bf16 pairs). Every wait is bounded; on a timeout the CTA keeps its barrier
+// schedule, sets TS_STATUS_TIMEOUT and frees its TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
