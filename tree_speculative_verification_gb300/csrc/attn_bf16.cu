@@ -410,8 +410,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
             for (int j = 0; j < NT; ++j) {
                 const float mu0 = m_run[j][0] == -INFINITY ? 0.f : m_run[j][0];
                 const float mu1 = m_run[j][1] == -INFINITY ? 0.f : m_run[j][1];
-                const float p0 = exp2f(__fmaf_rn(sacc[j][0], c, -mu0)), p1 = exp2f(__fmaf_rn(sacc[j][1], c, -mu1));
-                const float p2 = exp2f(__fmaf_rn(sacc[j][2], c, -mu0)), p3 = exp2f(__fmaf_rn(sacc[j][3], c, -mu1));
+                const float p0 = ex2(__fmaf_rn(sacc[j][0], c, -mu0)), p1 = ex2(__fmaf_rn(sacc[j][1], c, -mu1));
+                const float p2 = ex2(__fmaf_rn(sacc[j][2], c, -mu0)), p3 = ex2(__fmaf_rn(sacc[j][3], c, -mu1));
                 const __nv_bfloat162 b01 = __floats2bfloat162_rn(p0, p1), b23 = __floats2bfloat162_rn(p2, p3);
                 l_run[j][0] += p0 + p2;
                 l_run[j][1] += p1 + p3;

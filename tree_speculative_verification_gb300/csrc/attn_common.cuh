@@ -77,6 +77,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 2^x by the PTX ex2.approx.ftz.f32 instruction (results below 2^-126 flush to
+// zero, which no softmax sum notices; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float &lo_r, float &hi_r) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     lo_r = __bfloat162float(v.x);

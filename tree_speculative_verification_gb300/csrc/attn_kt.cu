@@ -249,13 +249,6 @@ __device__ __forceinline__ float reduce16(float (&v)[16]) {
     return v[0];
 }
 
-// 2^x with the SFU's approximate exp2 (flushes subnormal results to zero).
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
 #pragma unroll
                         for (int e = 0; e < 32 * NKB; e += 2) {
                             // the row sum takes the fp32 probabilities, P V their bf16 roundings
-                            const float p0 = exp2f(__fmaf_rn(sv[e], c, -mu)), p1 = exp2f(__fmaf_rn(sv[e + 1], c, -mu));
+                            const float p0 = ex2(__fmaf_rn(sv[e], c, -mu)), p1 = ex2(__fmaf_rn(sv[e + 1], c, -mu));
                             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                             pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&pb);
                             ls[(e >> 1) & 3] += p0 + p1;
