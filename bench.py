@@ -205,6 +205,20 @@ def _events(n, external):
     return [torch.cuda.Event(**kw) for _ in range(n)]
 
 
+def replica_rate(ms_per_step, units_per_step, dist=None, device="cpu"):
+    """Whole-job rate of N independent replicas (one per rank, no exchange): the
+    slowest rank's time per step (max over ranks) and every rank's units over it.
+    Returns (ms per step, units per second)."""
+    import torch
+    ws = 1
+    if dist is not None:
+        ws = dist.get_world_size()
+        t = torch.tensor([float(ms_per_step)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    return ms_per_step, ws * units_per_step / (ms_per_step * 1e-3)
+
+
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -380,22 +394,13 @@ def run_ours(args):
                     "kernel": api.attention_kernel(seq_w.B, seq_w.H, seq_w.n_max, seq_w.d, seq_w.L_max,
                                                    api.TS_BF16 if seq_w.dtype == "bf16" else api.TS_F32)}
         del sq, g
-    if dist:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    ms_per_step = ms / args.steps
-    value = ws * nodes_per_step / (ms_per_step * 1e-3)
+    ms_per_step, value = replica_rate(ms / args.steps, nodes_per_step, dist, device)
 
     # ---- end to end through the C ABI with host buffers: pinned inputs in, results out
     # every rank runs it (replicas); the slowest rank's time sets the job's figure
     barrier()
     e2e = measure_e2e(s, w, kind, args, stream)
-    if dist:
-        te = torch.tensor([e2e["ms_per_step"]], device=device)
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(te.item())
-    e2e["value"] = ws * nodes_per_step / (e2e["ms_per_step"] * 1e-3)
+    e2e["ms_per_step"], e2e["value"] = replica_rate(e2e["ms_per_step"], nodes_per_step, dist, device)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
