@@ -120,11 +120,18 @@ class DeviceStep:
         if self._side is None:
             self._side = torch.cuda.Stream(self.device)
             self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        # greedy verification (many small CTAs) forks after the append, so that the
+        # attention's CTAs are placed first; MSS (one large CTA per request) forks
+        # right after the build and keeps its few SMs while the attention fills the rest
+        late = (kind or self.w.verify) == "greedy"
+        if late:
+            self.append(main)
         self._fork.record(main)
         self._side.wait_event(self._fork)
         self.verify(kind, self._side)
         self._join.record(self._side)
-        self.append(main)
+        if not late:
+            self.append(main)
         self.attend(main)
         main.wait_event(self._join)
         self.commit(kind, main)
