@@ -172,6 +172,21 @@ ts_status tree_expand_topk(int32_t *tokens, const int32_t *root_token, const flo
                            cudaStream_t stream);
 
 /*
+ * tree_build_append -- tree_build in widths mode (an expansion tree, SpecInfer
+ * sec. 3) and kv_append (sec. 4.2) in one launch, for a dense cache: the tree
+ * arrays of t and the cache rows P + dfs(v) equal those of the two separate
+ * calls. Arguments as for the two calls; prefix_len is required. The copy does
+ * not wait for the tree arrays (an expansion tree's depth-first positions are
+ * arithmetic), which takes one launch off the step's critical path.
+ * A request with prefix_len[b] + n > L_max gets its tree arrays but no rows
+ * (TS_STATUS_INDEX).
+ */
+ts_status tree_build_append(const ts_tree *t, const int32_t *tokens, const int32_t *widths, int m,
+                            const int32_t *prefix_len, void *k_cache, void *v_cache, const void *k_new,
+                            const void *v_new, int H, int d, int L_max, ts_dtype dtype, uint32_t *status,
+                            cudaStream_t stream);
+
+/*
  * kv_append -- place the pass's fresh K/V in the shared cache in depth-first
  * order right after the verified prefix (SpecInfer sec. 4.2):
  *   cache[b][h][prefix_len[b] + dfs_of[v]][:] = new[b][v][h][:]

@@ -27,7 +27,7 @@ PAGE_KEYS = 64   # TS_PAGE_KEYS
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
            "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive",
-           "tree_expand_topk", "kv_append_paged", "tree_attention_paged", "kv_commit_paged")
+           "tree_expand_topk", "kv_append_paged", "tree_attention_paged", "kv_commit_paged", "tree_build_append")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -66,6 +66,7 @@ def load_library(path: str | None = None):
         "tree_build": [T, P, P, P, P, I, P, P, P],
         "tree_build_chains": [T, P, P, I, I, P, P, P, P, P, P],
         "kv_append": [P, P, P, P, P, T, I, I, I, I, P, P],
+        "tree_build_append": [T, P, P, I, P, P, P, P, P, I, I, I, I, P, P],
         "tree_attention": [P, P, P, P, P, T, I, I, I, I, F, P, Z, P, P],
         "verify_greedy": [P, P, P, P, P, T, I, P, Z, P, P],
         "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
@@ -159,6 +160,18 @@ def tree_build(tree: Tree, tokens, parent=None, n_nodes=None, widths=None, prefi
     _check(lib.tree_build(tree.c, _ptr(_i32(tokens, "tokens")), _ptr(_i32(parent, "parent")),
                           _ptr(_i32(n_nodes, "n_nodes")), w_arr, m, _ptr(_i32(prefix_len, "prefix_len")),
                           _ptr(status), _stream(stream)), "tree_build")
+
+
+def tree_build_append(tree: Tree, tokens, widths, prefix_len, k_cache, v_cache, k_new, v_new, status=None,
+                      stream=None):
+    """tree_build (widths mode) and kv_append in one launch (dense cache)."""
+    lib = load_library()
+    m = len(widths)
+    w_arr = (C.c_int32 * max(1, m))(*[int(k) for k in widths])
+    B, H, L_max, d = k_cache.shape
+    _check(lib.tree_build_append(tree.c, _ptr(_i32(tokens, "tokens")), w_arr, m, _ptr(_i32(prefix_len, "prefix_len")),
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), H, d, L_max,
+                                 _dtype(k_cache), _ptr(status), _stream(stream)), "tree_build_append")
 
 
 def tree_build_chains(tree: Tree, root_token, chains, tokens_out=None, p_row=None, q_row=None, prefix_len=None,

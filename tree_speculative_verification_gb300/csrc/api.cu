@@ -162,6 +162,25 @@ ts_status tree_build_chains(const ts_tree *t, const int32_t *root_token, const i
                        "tree_build_chains");
 }
 
+ts_status tree_build_append(const ts_tree *t, const int32_t *tokens, const int32_t *widths, int m,
+                            const int32_t *prefix_len, void *k_cache, void *v_cache, const void *k_new,
+                            const void *v_new, int H, int d, int L_max, ts_dtype dtype, uint32_t *status,
+                            cudaStream_t stream) {
+    ts_status st = check_tree(t, "tree_build_append");
+    if (st) return st;
+    if ((st = check_attn_shape("tree_build_append", t, H, d, L_max, dtype))) return st;
+    if (!tokens || !widths || !prefix_len || !k_cache || !v_cache || !k_new || !v_new)
+        return fail(TS_ERR_INVALID_ARG, "tree_build_append: NULL pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(TS_ERR_INVALID_ARG, "tree_build_append: caches and new K/V must be 16-byte aligned");
+    ts::WidthsParam w;
+    if (!widths_param(widths, m, t->n_max, w, "tree_build_append")) return TS_ERR_INVALID_ARG;
+    const int esize = dtype == TS_BF16 ? 2 : 4;
+    return cuda_result(ts::launch_build_append_widths(*t, tokens, w, prefix_len, k_cache, v_cache, k_new, v_new, H,
+                                                      d, L_max, esize, status, stream),
+                       "tree_build_append");
+}
+
 ts_status kv_append(void *k_cache, void *v_cache, const void *k_new, const void *v_new, const int32_t *prefix_len,
                     const ts_tree *t, int H, int d, int L_max, ts_dtype dtype, uint32_t *status,
                     cudaStream_t stream) {

@@ -153,13 +153,10 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_parent(ts_tree t, const int
 // depth-first position i, walks down from the root choosing child
 // (rest - 1) / sub[d + 1] at each depth, and gets its input id, depth, parent,
 // subtree end and ancestors without shared memory or barriers.
-__global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int32_t *tokens, WidthsParam w,
-                                                            const int32_t *prefix_len, uint32_t *status) {
-    const int b = blockIdx.x, i = threadIdx.x;
+// Tree arrays of request b, DFS position i (one thread per position).
+__device__ __forceinline__ void build_widths_node(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
+                                                  int P, int b, int i) {
     const int n = w.n, n_max = t.n_max, W = TS_MASK_WORDS(n_max);
-    pdl_wait();
-    pdl_trigger();
-    const int P = prefix_len ? prefix_len[b] : 0;
     const size_t o = (size_t)b * n_max + i;
     if (i < n) {
         int d = 0, pos = 0, par = -1, idx = 0;   // current node: depth, DFS position, parent position, index in level
@@ -203,7 +200,80 @@ __global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int
         for (int wd = 0; wd < W; ++wd) t.anc[o * W + wd] = 0u;
     }
     if (i == 0) t.n_nodes[b] = n;
+}
+
+__global__ void __launch_bounds__(kMaxNodes) k_build_widths(ts_tree t, const int32_t *tokens, WidthsParam w,
+                                                            const int32_t *prefix_len, uint32_t *status) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x;
+    build_widths_node(t, tokens, w, prefix_len ? prefix_len[b] : 0, b, threadIdx.x);
     (void)status;
+}
+
+// Depth-first position of the node with level-order id v of an expansion tree:
+// v sits at level d with index idx in it, whose mixed-radix digits c_0 .. c_{d-1}
+// (radices widths[0..d-1]) are the child ranks on its root path; every step
+// down passes the node itself and c_l whole subtrees of the level below.
+__device__ __forceinline__ int widths_dfs_of(const WidthsParam &w, int v) {
+    int d = 0;
+#pragma unroll
+    for (int l = 1; l <= 16; ++l)
+        if (l <= w.m && v >= w.level_start[l]) d = l;
+    int idx = v - w.level_start[d], pos = 0;
+    for (int l = d - 1; l >= 0; --l) {   // digits from the last level up
+        const int c = idx % w.width[l];
+        idx /= w.width[l];
+        pos += 1 + c * w.sub[l + 1];
+    }
+    return pos;
+}
+
+// tree_build for an expansion tree and kv_append in one launch: CTA (h, b)
+// copies head h of request b's new K/V rows to cache rows P + dfs(v) (the
+// positions are arithmetic, so the copy does not wait for the tree arrays),
+// and the CTAs of head 0 also write the tree arrays. The results equal the two
+// separate calls'.
+__global__ void __launch_bounds__(kMaxNodes) k_build_append_widths(ts_tree t, const int32_t *tokens, WidthsParam w,
+                                                                   const int32_t *prefix_len, uint4 *k_cache,
+                                                                   uint4 *v_cache, const uint4 *k_new,
+                                                                   const uint4 *v_new, int H, int row_vec, int L_max,
+                                                                   uint32_t *status) {
+    const int b = blockIdx.y, h = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int P = prefix_len[b], n = w.n;
+    if (h == 0) build_widths_node(t, tokens, w, P, b, threadIdx.x);
+    if (P < 0 || P + n > L_max) {
+        if (h == 0 && threadIdx.x == 0) flag(status, TS_STATUS_INDEX);
+        return;
+    }
+    __shared__ int dfs_s[kMaxNodes];
+    for (int v = threadIdx.x; v < n; v += kMaxNodes) dfs_s[v] = widths_dfs_of(w, v);
+    __syncthreads();
+    const size_t base_row = ((size_t)b * H + h) * L_max + P;
+    const int total = n * row_vec;
+    for (int base = threadIdx.x; base < total; base += 4 * kMaxNodes) {
+        uint4 kv[4], vv[4];
+        size_t dst[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int idx = base + k * kMaxNodes;
+            if (idx < total) {
+                const int v = idx / row_vec, c = idx - v * row_vec;
+                const size_t src = (((size_t)b * t.n_max + v) * H + h) * row_vec + c;
+                dst[k] = (base_row + dfs_s[v]) * row_vec + c;
+                kv[k] = __ldcs(k_new + src);
+                vv[k] = __ldcs(v_new + src);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (base + k * kMaxNodes < total) {
+                k_cache[dst[k]] = kv[k];
+                v_cache[dst[k]] = vv[k];
+            }
+    }
 }
 
 // Def. 3.2 merge, data-parallel: slot s = (chain c, position p). The slot
@@ -368,6 +438,16 @@ cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, co
 cudaError_t launch_tree_build_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s) {
     return launch(k_build_widths, dim3(t.B), dim3(kMaxNodes), 0, s, t, tokens, w, prefix_len, status);
+}
+
+cudaError_t launch_build_append_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
+                                       const int32_t *prefix_len, void *k_cache, void *v_cache, const void *k_new,
+                                       const void *v_new, int H, int d, int L_max, int esize, uint32_t *status,
+                                       cudaStream_t s) {
+    const int row_vec = d * esize / 16;
+    return launch(k_build_append_widths, dim3(H, t.B), dim3(kMaxNodes), 0, s, t, tokens, w, prefix_len,
+                  (uint4 *)k_cache, (uint4 *)v_cache, (const uint4 *)k_new, (const uint4 *)v_new, H, row_vec, L_max,
+                  status);
 }
 
 cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token, const int32_t *chains, int C,

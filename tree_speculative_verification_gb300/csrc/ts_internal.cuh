@@ -59,6 +59,10 @@ struct WidthsParam {
 cudaError_t launch_tree_build_parent(const ts_tree &t, const int32_t *tokens, const int32_t *parent,
                                      const int32_t *n_nodes, const int32_t *prefix_len,
                                      uint32_t *status, cudaStream_t s);
+cudaError_t launch_build_append_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
+                                       const int32_t *prefix_len, void *k_cache, void *v_cache, const void *k_new,
+                                       const void *v_new, int H, int d, int L_max, int esize, uint32_t *status,
+                                       cudaStream_t s);
 cudaError_t launch_tree_build_widths(const ts_tree &t, const int32_t *tokens, const WidthsParam &w,
                                      const int32_t *prefix_len, uint32_t *status, cudaStream_t s);
 cudaError_t launch_tree_build_chains(const ts_tree &t, const int32_t *root_token, const int32_t *chains,

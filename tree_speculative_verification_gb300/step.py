@@ -56,6 +56,7 @@ class DeviceStep:
         self.argmax = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
         self.ws_greedy = api.workspace(api.TS_OP_VERIFY_GREEDY, B, n_max=n_max, V=w.V, device=dev)
         self._side = None   # verification stream, created on first use
+        self._fused = w.tree_mode == "widths"   # tree_build_append applies
         self.attention = attention and w.q is not None
         if self.attention:
             bf = w.dtype == "bf16"
@@ -113,8 +114,8 @@ class DeviceStep:
         a second stream beside the KV append and the attention; the commit, which
         needs the accepted path and the appended rows, waits for both."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
-        self.build(main)
         if not self.attention:
+            self.build(main)
             self.verify(kind, main)
             return
         if self._side is None:
@@ -124,8 +125,13 @@ class DeviceStep:
         # attention's CTAs are placed first; MSS (one large CTA per request) forks
         # right after the build and keeps its few SMs while the attention fills the rest
         late = (kind or self.w.verify) == "greedy"
-        if late:
-            self.append(main)
+        if late and self._fused:   # expansion tree: tree_build and kv_append in one launch
+            api.tree_build_append(self.tree, self.tokens, self.w.widths, self.prefix_len, self.k_cache, self.v_cache,
+                                  self.k_new, self.v_new, self.status, main)
+        else:
+            self.build(main)
+            if late:
+                self.append(main)
         self._fork.record(main)
         self._side.wait_event(self._fork)
         self.verify(kind, self._side)
@@ -150,4 +156,6 @@ class DeviceStep:
             name = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max,
                                         api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
             attn = 2 + len(name.split("+"))
+            if kind == "greedy" and self._fused:
+                attn -= 1        # kv_append rides in the tree_build launch
         return 1 + attn + (2 if kind == "both" else 1)
