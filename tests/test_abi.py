@@ -144,3 +144,17 @@ def test_kernel_choice(lib, n_max, d, expect, monkeypatch):
 def test_kernel_override(lib, force, n_max, expect, monkeypatch):
     monkeypatch.setenv("TREESPEC_ATTN_KERNEL", force)
     assert api.attention_kernel(8, 32, n_max, 128, 2048 + n_max, api.TS_BF16).startswith(expect)
+
+
+def test_build_append_rejects_before_launch(lib):
+    """tree_build_append checks like tree_build (widths) and kv_append together."""
+    t = _tree(n_max=10)
+    p, bad = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    w = (C.c_int32 * 3)(2, 2, 1)     # 11 nodes > n_max
+    rc = lib.tree_build_append(C.byref(t), p, w, 3, p, p, p, p, p, 2, 128, 64, api.TS_BF16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"n_max" in lib.treespec_last_error()
+    w2 = (C.c_int32 * 2)(2, 2)       # 7 nodes
+    rc = lib.tree_build_append(C.byref(t), p, w2, 2, p, p, bad, p, p, 2, 128, 64, api.TS_BF16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
+    rc = lib.tree_build_append(C.byref(t), p, w2, 2, None, p, p, p, p, 2, 128, 64, api.TS_BF16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"NULL" in lib.treespec_last_error()
