@@ -1,11 +1,14 @@
 """Benchmark of one tree-verification step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama7b] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config opt30b] [--impl ours|reference]
 
 A step is the whole hot path over one batch of synthetic input, all through
 the C ABI: tree_build -> kv_append -> tree_attention -> verify -> kv_commit.
 Prints ONE JSON line (rank 0). Metric: verified tree nodes per second (the
 speculated-tree nodes, root included, that one step verifies), whole job.
+The headline workload is the largest single-GPU one (OPT-30B-shaped, 3008
+nodes and about 3 GB of K/V and logits per step); the line also carries the
+other four workloads measured in the same run (per_config).
 Under torchrun every rank runs an independent replica on its own GPU (the path
 needs no exchange); value = nodes of all ranks / max-over-ranks time.
 """
@@ -60,28 +63,44 @@ def attention_bytes(w) -> int:
     return kv + qo
 
 
-def _traffic_from_profile(w, kernel):
-    """dram bytes per attention launch from the committed ncu summary, only if the
-    summary is of the kernel this run launches and the kernel source is
-    unchanged since the capture (hash of attn_bf16.cu)."""
-    src = os.path.join(ROOT, "tree_speculative_verification_gb300", "csrc", "attn_bf16.cu")
-    prof = os.path.join(ROOT, "profiles", f"tree_attention_{w.name}.md")
-    try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        txt = open(prof).read()
-    except OSError:
-        return None
+def _profile_keys(path):
     kv = {}
-    for line in txt.splitlines():
-        if line.startswith("- ") and ":" in line:
-            k, _, v = line[2:].partition(":")
-            kv[k.strip()] = v.strip()
-    if kv.get("source_sha256_16") != h or kv.get("kernel") != kernel:
-        return None
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("- ") and ":" in line:
+                k, _, v = line[2:].partition(":")
+                kv[k.strip()] = v.strip()
+    return kv
+
+
+def _traffic_from_profile(w, kernel):
+    """DRAM bytes per full attention launch from a committed ncu summary under
+    profiles/: the summary must name this workload and the kernel this run
+    launches (`kernel`), and the hash of that kernel's source file (`source`)
+    must equal the one recorded at capture time (`source_sha256_16`).
+    Returns (bytes, summary file name) or (None, None)."""
+    pdir = os.path.join(ROOT, "profiles")
     try:
-        return float(kv["dram_bytes_per_full_launch"])
-    except (KeyError, ValueError):
-        return None
+        names = sorted(os.listdir(pdir))
+    except OSError:
+        return None, None
+    for name in names:
+        if not name.endswith(".md"):
+            continue
+        try:
+            kv = _profile_keys(os.path.join(pdir, name))
+        except OSError:
+            continue
+        if kv.get("kernel") != kernel or kv.get("workload") != w.name or "source" not in kv:
+            continue
+        try:
+            src = os.path.join(ROOT, kv["source"])
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            if kv.get("source_sha256_16") == h:
+                return float(kv["dram_bytes_per_full_launch"]), name
+        except (OSError, KeyError, ValueError):
+            continue
+    return None, None
 
 
 class ClockSampler:
@@ -153,10 +172,11 @@ def _oracle_tree(w):
     return w.parent, w.tokens, w.n_nodes, None, w.q_row
 
 
-def run_oracle_sample(w, heads: int, verify: bool = True):
-    """One bounded oracle pass: attention rows of request 0 for `heads` heads,
-    then (optionally) the step's verifier on every request. Returns seconds
-    spent in attention and in verification."""
+def run_oracle_sample(w, heads: int, verify: bool = True, nthreads: int = 0):
+    """One bounded oracle pass: attention rows of request 0 for `heads` heads
+    (on `nthreads` threads, 0 = all cores), then (optionally) the step's
+    verifier on every request. Returns seconds spent in attention and in
+    verification."""
     import oracle
     parent, tokens, n_nodes, p_row, q_row = _oracle_tree(w)
     n0 = int(n_nodes[0])
@@ -164,7 +184,7 @@ def run_oracle_sample(w, heads: int, verify: bool = True):
     t0 = time.perf_counter()
     if w.q is not None and heads > 0:
         oracle.tree_attention_rows(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.prefix_len, n_nodes, parent, rows,
-                                   nthreads=0)
+                                   nthreads=nthreads)
     t1 = time.perf_counter()
     if verify:
         if w.verify == "naive":
@@ -179,12 +199,33 @@ def run_oracle_sample(w, heads: int, verify: bool = True):
     return t1 - t0, t2 - t1, n_nodes
 
 
-def oracle_nodes_per_s(w, budget_s: float):
-    """Time the oracle on a bounded sample and extrapolate to the whole step."""
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo, or lscpu on Arm hosts)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_nodes_per_s(w, budget_s: float, nthreads: int = 0):
+    """Time the oracle on a bounded sample and extrapolate to the whole step.
+    nthreads: attention threads (0 = all cores; verification is serial C)."""
     import oracle
-    ta, tv, n_nodes = run_oracle_sample(w, heads=1)
+    ta, tv, n_nodes = run_oracle_sample(w, heads=1, nthreads=nthreads)
     heads = max(1, min(w.H, int(budget_s / max(ta, 1e-4))))
-    ta, tv2, n_nodes = run_oracle_sample(w, heads=heads, verify=False)
+    ta, tv2, n_nodes = run_oracle_sample(w, heads=heads, verify=False, nthreads=nthreads)
     # attention cost per node-head from the sample, applied to every node-head of the step
     per_node_head = ta / (heads * int(n_nodes[0]))
     # rows of longer prefixes cost proportionally more keys
@@ -194,7 +235,7 @@ def oracle_nodes_per_s(w, budget_s: float):
     sample = (f"oracle tree attention for request 0 ({int(n_nodes[0])} nodes) x {heads} of {w.H} heads "
               f"({ta:.2f} s), scaled by key count to all {w.B} requests and heads; oracle verification of all "
               f"{w.B} requests ({tv:.2f} s)")
-    return float(np.sum(n_nodes)) / t_step, t_step, oracle.num_threads(), sample
+    return float(np.sum(n_nodes)) / t_step, t_step, (nthreads or oracle.num_threads()), sample
 
 
 def _events(n, external):
@@ -217,6 +258,14 @@ def replica_rate(ms_per_step, units_per_step, dist=None, device="cpu"):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
     return ms_per_step, ws * units_per_step / (ms_per_step * 1e-3)
+
+
+def config_dict(w, name, kind, ws, scale_down=1):
+    """The workload description both arms print (identical for the same run)."""
+    return {"workload": DESCR[name] + (f" (batch and long prefix / {scale_down})" if scale_down > 1 else ""),
+            "name": name, "batch": w.B, "heads": w.H, "head_dim": w.d, "vocab": w.V,
+            "nodes_per_step": int(np.sum(w.n_nodes_dev)), "verify": kind,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
 
 
 def _dist_env():
@@ -249,10 +298,121 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DESCR[args.config], "name": args.config},
+            "config": config_dict(w, args.config, w.verify, args.gpus),
             "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _load_step(name, args, device, verify=None):
+    from tree_speculative_verification_gb300 import api, workloads
+    from tree_speculative_verification_gb300.step import DeviceStep
+    w = workloads.make(name, scale_down=args.scale_down)
+    if verify:
+        if verify in ("mss", "both") and w.ssm is None:
+            raise SystemExit(f"--verify {verify}: the {name} workload has no drafter distributions")
+        w.verify = verify
+    s = DeviceStep(w, device)
+    s.run(w.verify)
+    import torch
+    torch.cuda.synchronize()
+    w.n_nodes_dev = s.tree.n_nodes.cpu().numpy()
+    if s.status.item() not in (0, api.STATUS_ZERO_RESID):
+        raise RuntimeError(f"{name}: device status {s.status.item()} after the first step")
+    return w, s
+
+
+def _timed_graphs(s, kind, K, device, stream, eager=False):
+    """The K steps as one CUDA graph (the step's library calls; the graph
+    removes the host launch overhead between them) with events at its two ends
+    only -- an event-record node between two kernels of a graph costs a few
+    microseconds -- and two more graphs of K back-to-back launches of the
+    attention call and of the verify call alone on the same inputs (the time
+    between two launches counts, so those figures are conservative).
+    Returns (events per pass, a function replaying a pass, launch mode)."""
+    import torch
+    passes = {
+        "step": lambda: [s.run(kind) for _ in range(K)],
+        "attend": lambda: [s.attend() for _ in range(K)],
+        "verify": lambda: [s.verify(kind) for _ in range(K)],
+    }
+    evs = {k: _events(2, not eager) for k in passes}
+    graphs, mode = None, "eager launches"
+    if not eager:
+        try:
+            graphs = {}
+            for k, body in passes.items():
+                g = torch.cuda.CUDAGraph()
+                cs = torch.cuda.Stream(device)
+                cs.wait_stream(stream)
+                with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+                    cur = torch.cuda.current_stream(device)
+                    evs[k][0].record(cur)
+                    body()
+                    evs[k][1].record(cur)
+                stream.wait_stream(cs)
+                g.replay()
+                torch.cuda.synchronize()
+                graphs[k] = g
+            mode = "CUDA graph of the K steps"
+        except Exception as exc:     # no graph support for event nodes: time eager launches
+            graphs = None
+            mode = f"eager launches ({type(exc).__name__} capturing a graph)"
+            torch.cuda.synchronize()
+            evs = {k: _events(2, False) for k in passes}
+
+    def replay(k="step"):
+        if graphs is not None:
+            graphs[k].replay()
+        else:
+            evs[k][0].record(stream)
+            passes[k]()
+            evs[k][1].record(stream)
+
+    return evs, replay, mode
+
+
+def _roofline(w, t_att_ms, kernel):
+    peak, peak_kind = _peaks()
+    abytes = attention_bytes(w)
+    achieved = abytes / (t_att_ms * 1e-3) / 1e9
+    traffic, prof = _traffic_from_profile(w, kernel)
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "traffic_source": prof, "kernel": f"tree_attention ({kernel})",
+            "algorithmic_bytes_per_launch": abytes, "peak_kind": peak_kind, "avg_launch_us": t_att_ms * 1e3}
+
+
+def measure_other_config(name, args, device, stream):
+    """A workload other than the headline one, measured in the same run with
+    the same method (graphs of K steps and of K back-to-back attention /
+    verify launches); no end-to-end leg, no CPU baseline."""
+    import torch
+    from tree_speculative_verification_gb300 import api
+    w, s = _load_step(name, args, device)
+    kind = w.verify
+    K = max(10, min(args.steps, 100))
+    for _ in range(3):
+        s.run(kind)
+    torch.cuda.synchronize()
+    evs, replay, _ = _timed_graphs(s, kind, K, device, stream, args.eager)
+    out = {}
+    for k in ("step", "attend", "verify"):
+        replay(k)
+        torch.cuda.synchronize()
+        replay(k)
+        torch.cuda.synchronize()
+        out[k] = evs[k][0].elapsed_time(evs[k][1]) / K
+    nodes = int(w.n_nodes_dev.sum())
+    kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
+    roof = _roofline(w, out["attend"], kernel)
+    line = {"value": nodes / (out["step"] * 1e-3), "unit": "nodes/s", "ms_per_step": out["step"],
+            "nodes_per_step": nodes, "attention_ms": out["attend"], "verify_ms": out["verify"], "verify": kind,
+            "attention_kernel": kernel, "roofline_frac": roof["frac"], "attention_gbs": roof["achieved"],
+            "accepted_tokens_per_step": s.accepted(kind), "steps": K, "workload": DESCR[name]}
+    del s, w
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_ours(args):
@@ -266,78 +426,23 @@ def run_ours(args):
     device = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(device)
     from tree_speculative_verification_gb300 import api, workloads
-    from tree_speculative_verification_gb300.step import DeviceStep
     api.load_library()
-    w = workloads.make(args.config, scale_down=args.scale_down)
-    if args.verify:
-        if args.verify in ("mss", "both") and w.ssm is None:
-            raise SystemExit(f"--verify {args.verify}: the {args.config} workload has no drafter distributions")
-        w.verify = args.verify
-    s = DeviceStep(w, device)
     stream = torch.cuda.current_stream(device)
+    w, s = _load_step(args.config, args, device, args.verify)
     kind = w.verify
-    s.run(kind)
-    torch.cuda.synchronize()
-    w.n_nodes_dev = s.tree.n_nodes.cpu().numpy()
     nodes_per_step = int(w.n_nodes_dev.sum())
     accepted_per_step = s.accepted(kind)
-    if s.status.item() not in (0, api.STATUS_ZERO_RESID):
-        raise RuntimeError(f"device status {s.status.item()} after the first step")
 
     def barrier():
         if dist:
             dist.barrier()
 
-    # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream).
-    # The K steps are captured once into a CUDA graph (each step is the same five
-    # library calls; the graph removes the host launch overhead between them),
-    # with events at its two ends only: an event-record node between two kernels
-    # of a graph costs a few microseconds. The attention and verify durations
-    # come from two more timed passes, each a graph of K back-to-back launches of
-    # that one call on the same inputs (events at the ends; the time between two
-    # launches counts, so the figure is conservative).
+    # ---- warm-up, then K timed steps (device time, CUDA events on the launch stream)
     for _ in range(args.warmup):
         s.run(kind)
     torch.cuda.synchronize()
     K = args.steps
-    passes = {
-        "step": lambda cur: [s.run(kind) for _ in range(K)],
-        "attend": lambda cur: [s.attend() for _ in range(K)],
-        "verify": lambda cur: [s.verify(kind) for _ in range(K)],
-    }
-    evs = {k: _events(2, not args.eager) for k in passes}
-    graphs, launch_mode = None, "eager launches"
-    if not args.eager:
-        try:
-            graphs = {}
-            for k, body in passes.items():
-                g = torch.cuda.CUDAGraph()
-                cs = torch.cuda.Stream(device)
-                cs.wait_stream(stream)
-                with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
-                    cur = torch.cuda.current_stream(device)
-                    evs[k][0].record(cur)
-                    body(cur)
-                    evs[k][1].record(cur)
-                stream.wait_stream(cs)
-                g.replay()
-                torch.cuda.synchronize()
-                graphs[k] = g
-            launch_mode = "CUDA graph of the K steps"
-        except Exception as exc:     # no graph support for event nodes: time eager launches
-            graphs = None
-            launch_mode = f"eager launches ({type(exc).__name__} capturing a graph)"
-            torch.cuda.synchronize()
-            evs = {k: _events(2, False) for k in passes}
-
-    def timed_pass(k="step"):
-        if graphs is not None:
-            graphs[k].replay()
-        else:
-            evs[k][0].record(stream)
-            passes[k](stream)
-            evs[k][1].record(stream)
-
+    evs, timed_pass, launch_mode = _timed_graphs(s, kind, K, device, stream, args.eager)
     sampler = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
     t_load0 = time.time()
     while time.time() - t_load0 < 0.6:      # keep the GPU loaded while the sampler starts
@@ -364,36 +469,7 @@ def run_ours(args):
     t_ver = evs["verify"][0].elapsed_time(evs["verify"][1]) / K
     seq_line = None
     if args.sequence_baseline and rank == 0:
-        # SpecInfer Fig. 4 (left) / Fig. 11: one sequence and one prefix copy per
-        # root-to-leaf path, the same attention call on the chains
-        seq_w, path_nodes = workloads.sequence_batch(w)
-        seq_w.n_nodes_dev = seq_w.n_nodes
-        sq = DeviceStep(seq_w, device)
-        sq.build()
-        sq.append()
-        torch.cuda.synchronize()
-        ge = _events(2, True)
-        g = torch.cuda.CUDAGraph()
-        cs = torch.cuda.Stream(device)
-        cs.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
-            cur = torch.cuda.current_stream(device)
-            ge[0].record(cur)
-            for _ in range(K):
-                sq.attend()
-            ge[1].record(cur)
-        stream.wait_stream(cs)
-        g.replay()
-        torch.cuda.synchronize()
-        g.replay()
-        torch.cuda.synchronize()
-        t_seq = ge[0].elapsed_time(ge[1]) / K
-        seq_line = {"paths": int(seq_w.B), "path_nodes": int(seq_w.n_nodes.sum()), "attention_ms": t_seq,
-                    "algorithmic_bytes_per_launch": attention_bytes(seq_w),
-                    "tree_speedup": t_seq / t_att,
-                    "kernel": api.attention_kernel(seq_w.B, seq_w.H, seq_w.n_max, seq_w.d, seq_w.L_max,
-                                                   api.TS_BF16 if seq_w.dtype == "bf16" else api.TS_F32)}
-        del sq, g
+        seq_line = measure_sequence_baseline(w, K, device, stream, t_att)
     ms_per_step, value = replica_rate(ms / args.steps, nodes_per_step, dist, device)
 
     # ---- end to end through the C ABI with host buffers: pinned inputs in, results out
@@ -405,41 +481,84 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return
-    peak, peak_kind = _peaks()
-    abytes = attention_bytes(w)
-    achieved = abytes / (t_att * 1e-3) / 1e9
     kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": _traffic_from_profile(w, kernel), "kernel": f"tree_attention ({kernel})",
-            "algorithmic_bytes_per_launch": abytes, "peak_kind": peak_kind,
-            "avg_launch_us": t_att * 1e3}
+    roof = _roofline(w, t_att, kernel)
+    launches = args.steps * s.launches_per_step(kind)
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    host_w = w
+    del s
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    per_config = None
+    if ws == 1 and not args.no_per_config and args.scale_down == 1:
+        per_config = {}
+        for name in workloads.CONFIG_NAMES:
+            if name != args.config:
+                per_config[name] = measure_other_config(name, args, device, stream)
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        v, t_step, cores, sample = oracle_nodes_per_s(w, 12.0)
-        cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": sample}
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+        v, t_step, cores, sample = oracle_nodes_per_s(host_w, 12.0)
+        v1, t1, _, sample1 = oracle_nodes_per_s(host_w, 6.0, nthreads=1)
+        cpu = {"value": v, "unit": "nodes/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "cpu_model": cpu_model(),
+               "single_thread": {"value": v1, "unit": "nodes/s", "cores": 1, "sample": sample1}}
     line = {"metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": DESCR[args.config] + (f" (batch and long prefix / {args.scale_down})"
-                                                         if args.scale_down > 1 else ""),
-                       "name": args.config, "batch": w.B, "heads": w.H,
-                       "head_dim": w.d, "vocab": w.V, "nodes_per_step": nodes_per_step,
-                       "verify": kind, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "launch": launch_mode,
+            "config": config_dict(w, args.config, kind, ws, args.scale_down),
+            "timing": {"launch": launch_mode,
                        "kernel_timing": "attention and verify durations from graphs of K back-to-back launches "
                                         "of that call on the same inputs, events at both ends",
-                       "l2": f"inputs larger than L2: {abytes / 2**20:.0f} MiB of K/V+Q per step vs 129 MiB"},
+                       "l2": f"inputs larger than L2: {attention_bytes(w) / 2**20:.0f} MiB of K/V+Q per step vs "
+                             f"129 MiB"},
             "nodes_per_s_attn_verify": ws * nodes_per_step / ((t_att + t_ver) * 1e-3),
             "attention_ms": t_att, "verify_ms": t_ver,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "accepted_tokens_per_step": accepted_per_step,
             **({"sequence_baseline": seq_line} if seq_line else {}),
             "accepted_tokens_per_s": ws * accepted_per_step / (ms_per_step * 1e-3),
-            "gpu_launches": args.steps * s.launches_per_step(kind)}
+            "gpu_launches": launches,
+            **({"per_config": per_config} if per_config else {})}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def measure_sequence_baseline(w, K, device, stream, t_att):
+    """SpecInfer Fig. 4 (left) / Fig. 11: one sequence and one prefix copy per
+    root-to-leaf path, the same attention call on the chains."""
+    import torch
+    from tree_speculative_verification_gb300 import api, workloads
+    from tree_speculative_verification_gb300.step import DeviceStep
+    seq_w, path_nodes = workloads.sequence_batch(w)
+    seq_w.n_nodes_dev = seq_w.n_nodes
+    sq = DeviceStep(seq_w, device)
+    sq.build()
+    sq.append()
+    torch.cuda.synchronize()
+    ge = _events(2, True)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(device)
+    cs.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+        cur = torch.cuda.current_stream(device)
+        ge[0].record(cur)
+        for _ in range(K):
+            sq.attend()
+        ge[1].record(cur)
+    stream.wait_stream(cs)
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    t_seq = ge[0].elapsed_time(ge[1]) / K
+    line = {"paths": int(seq_w.B), "path_nodes": int(seq_w.n_nodes.sum()), "attention_ms": t_seq,
+            "algorithmic_bytes_per_launch": attention_bytes(seq_w),
+            "tree_speedup": t_seq / t_att,
+            "kernel": api.attention_kernel(seq_w.B, seq_w.H, seq_w.n_max, seq_w.d, seq_w.L_max,
+                                           api.TS_BF16 if seq_w.dtype == "bf16" else api.TS_F32)}
+    del sq, g
+    return line
 
 
 def measure_e2e(s, w, kind, args, stream):
@@ -537,9 +656,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="llama7b", choices=sorted(DESCR))
+    ap.add_argument("--config", default="opt30b", choices=sorted(DESCR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other four workloads (per_config)")
     ap.add_argument("--sequence-baseline", action="store_true",
                     help="also time attention as one sequence per root-to-leaf path (SpecInfer Fig. 4 left)")
     ap.add_argument("--verify", default=None, choices=["greedy", "mss", "naive", "both"],

@@ -206,11 +206,14 @@ ts_status kv_append(void *k_cache, void *v_cache, const void *k_new, const void 
  * the ancestor-or-self bitmask of *t, tested in registers; no N x N tensor.
  * q, out [B][n_max][H][d]; caches [B][H][L_max][d] as filled by kv_append.
  * scale <= 0 selects 1/sqrt(d). bf16: fp32 accumulation, bf16 output;
- * fp32: fp32 throughout. Split-KV over the key axis; the partial results go
- * to ws (ws_bytes >= treespec_workspace_size(TS_OP_ATTENTION, ...)); the last
- * CTA of each (b, h) merges them, so one launch. ws must be zero-filled
- * before its first use (treespec_workspace_init); calls leave it so.
- * Calls that share one ws must not overlap on the GPU.
+ * fp32: fp32 throughout. ws (ws_bytes >= treespec_workspace_size(
+ * TS_OP_ATTENTION, ...)) holds what the chosen kernel shares between its CTAs:
+ * for the split-KV kernel the partial results of the key splits and the
+ * per-(b, h) counters by which the last CTA of each (b, h) finds that it
+ * merges them (one launch); for the persistent kernel the queue its CTAs take
+ * (request, head) items from. ws must be zero-filled before its first use
+ * (treespec_workspace_init); calls leave it so. Calls that share one ws must
+ * not overlap on the GPU.
  */
 ts_status tree_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max,
@@ -250,15 +253,22 @@ ts_status verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_cou
  *                 child v is tested against row q_row[b][v]
  *   uniforms      [B][2][n_max] fp32 in [0, 1)
  *   temperature   > 0, divides the target logits
- * Outputs as verify_greedy. Arithmetic: fp32 elementwise, compensated sums
- * combined in fp64. A non-finite value met on the walk empties the request.
- * No workspace.
+ * Outputs as verify_greedy, plus
+ *   out_lowmargin [B] (may be NULL) the number of decisions of the request's
+ *                 walk whose margin, as computed here, is below 1e-6: an accept
+ *                 test with |u - a| < 1e-6, or a final sample whose u * S lies
+ *                 within 1e-6 * S of the cumulative sums on either side of the
+ *                 drawn token (S the residual's total). Such a decision may
+ *                 differ from one taken in exact arithmetic; a request with a
+ *                 count of 0 took every decision with at least that margin.
+ * Arithmetic: fp32 elementwise, compensated sums combined in fp64. A
+ * non-finite value met on the walk empties the request. No workspace.
  */
 ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
-                     const float *target_logits, const int32_t *p_row, int NP,
-                     const float *ssm_probs, const int32_t *q_row, int NQ, const float *uniforms,
-                     float temperature, const ts_tree *t, int V, uint32_t *status,
-                     cudaStream_t stream);
+                     int32_t *out_lowmargin, const float *target_logits, const int32_t *p_row,
+                     int NP, const float *ssm_probs, const int32_t *q_row, int NQ,
+                     const float *uniforms, float temperature, const ts_tree *t, int V,
+                     uint32_t *status, cudaStream_t stream);
 
 /*
  * verify_naive -- naive sampling (SpecInfer sec. 4.3, the verifier that
@@ -267,12 +277,12 @@ ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
  * with uniforms[b][1][u] (the first x, by id, with C(x) > u * sum p); if a
  * child of u (in input order) has token x, accept it and continue there,
  * else append x and stop. Arguments as verify_mss without the drafter rows;
- * uniforms[b][0][*] are not read. Same outputs, status bits and
- * floating-point rules as verify_mss.
+ * uniforms[b][0][*] are not read. Same outputs (out_lowmargin counts the
+ * samples), status bits and floating-point rules as verify_mss.
  */
-ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *target_logits,
-                       const int32_t *p_row, int NP, const float *uniforms, float temperature,
-                       const ts_tree *t, int V, uint32_t *status, cudaStream_t stream);
+ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                       const float *target_logits, const int32_t *p_row, int NP, const float *uniforms,
+                       float temperature, const ts_tree *t, int V, uint32_t *status, cudaStream_t stream);
 
 /*
  * kv_commit -- keep the accepted path's K/V (SpecInfer sec. 4.2: only the
@@ -345,9 +355,9 @@ size_t treespec_workspace_size(ts_op op, int B, int H, int n_max, int d, int L_m
 
 /*
  * Name of the kernel tree_attention launches for these sizes on the current
- * device ("k_attn_f32", "k_attn_bf16<D,NT,NG,KS>", "k_attn_tc" or
- * "k_attn_tp"), as chosen by the same plan the launch uses (including the
- * TREESPEC_ATTN_* environment overrides). Static string owned by the
+ * device ("k_attn_f32", "k_attn_bf16<D,NT,NG,KS>" or "k_attn_tq"), as chosen
+ * by the same plan the launch uses (including the TREESPEC_ATTN_KERNEL and
+ * TREESPEC_ATTN_SPLITS environment overrides). Static string owned by the
  * library; "" for sizes tree_attention would reject. No GPU work.
  */
 const char *treespec_attention_kernel(int B, int H, int n_max, int d, int L_max, ts_dtype dtype);

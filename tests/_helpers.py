@@ -85,9 +85,36 @@ def attention_error(step, w, n_nodes, parent, rows):
     ref = oracle.tree_attention_rows(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache, w.prefix_len, n_nodes, parent,
                                      rows, nthreads=0)
     out = step.out.float().cpu().numpy()
-    got = np.stack([out[b, v, h] for b, h, v in rows]).astype(np.float64)
+    got = out[rows[:, 0], rows[:, 2], rows[:, 1]].astype(np.float64)
     return float(np.max(np.abs(got - ref))), got, ref
 
 
 def torch_sync():
     torch.cuda.synchronize()
+
+
+def low_margin_prob(logits_row, T=1.0, eps=1e-6):
+    """Probability that an inverse-CDF draw u * S from p = softmax(logits / T)
+    lands within eps * S of a cumulative-sum boundary: the length of the union
+    of the windows [C(x) - eps, C(x) + eps] inside [0, 1). The expected count
+    of low-margin draws, from which the exclusion bounds of the sampling
+    verifiers' parity checks are derived."""
+    z = np.asarray(logits_row, np.float64) / T
+    p = np.exp(z - z.max())
+    c = np.concatenate([[0.0], np.cumsum(p / p.sum())])
+    lo, hi = np.maximum(c - eps, 0.0), np.minimum(c + eps, 1.0)
+    gap_start = lo[1:] > np.maximum.accumulate(hi)[:-1]       # a window that starts a new run
+    run_id = np.concatenate([[0], np.cumsum(gap_start)])
+    starts = np.full(run_id[-1] + 1, np.inf)
+    ends = np.zeros(run_id[-1] + 1)
+    np.minimum.at(starts, run_id, lo)
+    np.maximum.at(ends, run_id, hi)
+    return float(np.sum(ends - starts))
+
+
+def exclusion_bound(probs):
+    """At most this many requests may hold a low-margin decision: the expected
+    number (sum of per-request probabilities) plus four standard deviations of
+    the binomial-like count, plus 2."""
+    e = float(np.sum(probs))
+    return e + 4.0 * np.sqrt(e) + 2.0

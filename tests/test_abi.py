@@ -86,7 +86,7 @@ def test_workspace_too_small(lib):
 def test_mss_bad_temperature(lib):
     t = _tree()
     p = C.c_void_p(0x10000)
-    rc = lib.verify_mss(p, p, p, p, None, 8, p, p, 1, p, 0.0, C.byref(t), 16, None, None)
+    rc = lib.verify_mss(p, p, p, None, p, None, 8, p, p, 1, p, 0.0, C.byref(t), 16, None, None)
     assert rc == api.TS_ERR_INVALID_ARG and b"temperature" in lib.treespec_last_error()
 
 
@@ -132,15 +132,15 @@ def test_binding_fails_loudly_without_library(tmp_path):
 ])
 def test_kernel_choice(lib, n_max, d, expect, monkeypatch):
     """attn_plan's default choice is host logic: the same without a GPU."""
-    for var in ("TREESPEC_ATTN_KERNEL", "TREESPEC_ATTN_SPLITS", "TREESPEC_ATTN_PERSISTENT"):
+    for var in ("TREESPEC_ATTN_KERNEL", "TREESPEC_ATTN_SPLITS"):
         monkeypatch.delenv(var, raising=False)
     name = api.attention_kernel(8, 32, n_max, d, 2048 + n_max, api.TS_BF16)
     assert name.startswith(expect), name
     assert api.attention_kernel(8, 32, n_max, d, 2048 + n_max, api.TS_F32) == "k_attn_f32"
 
 
-@pytest.mark.parametrize("force,n_max,expect", [("mma", 47, "k_attn_bf16<"), ("tc", 47, "k_attn_tc"),
-                                                 ("tq", 21, "k_attn_tq"), ("kt", 21, "k_attn_kt")])
+@pytest.mark.parametrize("force,n_max,expect", [("mma", 47, "k_attn_bf16<"), ("tq", 21, "k_attn_tq"),
+                                                 ("mma", 21, "k_attn_bf16<")])
 def test_kernel_override(lib, force, n_max, expect, monkeypatch):
     monkeypatch.setenv("TREESPEC_ATTN_KERNEL", force)
     assert api.attention_kernel(8, 32, n_max, 128, 2048 + n_max, api.TS_BF16).startswith(expect)
@@ -158,3 +158,32 @@ def test_build_append_rejects_before_launch(lib):
     assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
     rc = lib.tree_build_append(C.byref(t), p, w2, 2, None, p, p, p, p, 2, 128, 64, api.TS_BF16, None, None)
     assert rc == api.TS_ERR_INVALID_ARG and b"NULL" in lib.treespec_last_error()
+
+
+def test_noalloc_rejects_before_touching_the_device(lib):
+    """tree_attention_noalloc runs every check of tree_attention before it looks
+    up or clears its scratch: with no GPU here, any device call would return
+    TS_ERR_CUDA, so an argument error coming back as TS_ERR_INVALID_ARG (or
+    TS_ERR_UNSUPPORTED) shows that nothing was enqueued."""
+    t = _tree()
+    p, bad = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    rc = lib.tree_attention_noalloc(None, p, p, p, p, C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"NULL" in lib.treespec_last_error()
+    rc = lib.tree_attention_noalloc(p, p, bad, p, p, C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
+    rc = lib.tree_attention_noalloc(p, p, p, p, None, C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG
+    rc = lib.tree_attention_noalloc(p, p, p, p, p, C.byref(t), 4, 96, 64, api.TS_BF16, 0.0, None, None)
+    assert rc == api.TS_ERR_UNSUPPORTED
+    rc = lib.tree_attention_noalloc(p, p, p, p, p, None, 4, 128, 64, api.TS_BF16, 0.0, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"tree" in lib.treespec_last_error()
+
+
+@pytest.mark.parametrize("B,H,n_max", [(32768, 128, 33), (8, 32, 64), (64, 56, 47)])
+def test_persistent_kernel_workspace_is_its_queue(lib, B, H, n_max, monkeypatch):
+    """The persistent tcgen05 plan keeps only its item queue in the workspace,
+    whatever the batch (no per-(request, head) counters), so the scratch-free
+    entry point's clear stays inside the plan's bytes even at B*H > 2^21."""
+    monkeypatch.delenv("TREESPEC_ATTN_KERNEL", raising=False)
+    assert api.attention_kernel(B, H, n_max, 128, 64 + n_max, api.TS_BF16) == "k_attn_tq"
+    assert api.workspace_size(api.TS_OP_ATTENTION, B, H, n_max, 128, 64 + n_max, 1) == 256

@@ -5,7 +5,11 @@ fp32 accumulation, <= 1e-4 for fp32 inputs.
 Small cases cover every kernel variant (node counts 1..256), several key tiles
 with ragged tails, ragged and empty prefixes, and forced key splits; the five
 workloads run at full size in the launch configuration the benchmark times,
-checked on sampled rows."""
+checked on every output row (every request, head and node).
+
+Tolerance for inputs scaled by s (value_scale): every error term -- the bf16
+rounding of the output and of the probabilities that multiply V -- is
+proportional to the magnitude of the values, so the bound is s * 2e-2."""
 import os
 
 import numpy as np
@@ -17,7 +21,7 @@ from tree_speculative_verification_gb300 import api
 from tree_speculative_verification_gb300.step import DeviceStep, to_device
 from tree_speculative_verification_gb300.workloads import f32_to_bf16_bits
 
-from _helpers import attention_error, oracle_tree, sample_rows, workload
+from _helpers import attention_error, oracle_tree, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -102,7 +106,8 @@ def test_bf16_large_scores_stable():
     # scores of magnitude ~100 exercise the running-max rescaling
     rng = np.random.default_rng(8)
     err, _, _ = _run_case(rng, 1, 2, 128, 21, prefix=[700], value_scale=3.0)
-    assert err <= 5 * TOL_BF16, err    # bf16 rounding of inputs of size ~3 scales the error
+    print(f"value scale 3: max-abs error {err:.4f}")
+    assert err <= 3.0 * TOL_BF16, err    # the bound scales with the magnitude of V
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -123,18 +128,33 @@ def test_f32_tiny_workload():
     assert err <= TOL_F32, err
 
 
-@pytest.mark.parametrize("name", ["llama7b", "merge", "long65b", "opt30b"])
-def test_full_size_sampled(name):
+def full_size_every_row(name, kernel=None):
+    """Every output row of the workload at full size against the oracle."""
     w = workload(name)
     s = DeviceStep(w)
     s.build(); s.append(); s.attend()
     torch.cuda.synchronize()
     assert s.status.item() == 0
+    if kernel:
+        assert api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16).startswith(kernel)
     parent, tokens, n_nodes, _, _ = oracle_tree(w)
-    rows = sample_rows(w, n_nodes, 48, seed=len(name))
-    err, _, _ = attention_error(s, w, n_nodes, parent, rows)
+    rows = oracle.all_rows(w.B, w.H, n_nodes)
+    err, got, _ = attention_error(s, w, n_nodes, parent, rows)
+    print(f"[{name}] {len(rows)} rows, max-abs error {err:.4g}")
     assert err <= TOL_BF16, err
-    # every output row of every real node is finite
-    out = s.out.float()
-    for b in range(w.B):
-        assert torch.isfinite(out[b, : int(n_nodes[b])]).all()
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("name", ["llama7b", "merge", "long65b", "opt30b"])
+def test_full_size_every_row(name):
+    """The kernel the benchmark times (mma.sync for llama7b and merge, the
+    persistent tcgen05 kernel for long65b and opt30b)."""
+    full_size_every_row(name)
+
+
+@pytest.mark.parametrize("name", ["llama7b", "merge", "opt30b"])
+def test_full_size_every_row_mma(name, monkeypatch):
+    """The mma.sync kernel forced onto the workloads (longest-first dispatch of
+    the ragged merge prefixes; opt30b: 3584 (request, head) CTAs of 47 nodes)."""
+    monkeypatch.setenv("TREESPEC_ATTN_KERNEL", "mma")
+    full_size_every_row(name, "k_attn_bf16<")

@@ -7,8 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from test_gpu_attention import TOL_BF16, _run_case
-from _helpers import attention_error, oracle_tree, sample_rows, workload
+from test_gpu_attention import TOL_BF16, _run_case, full_size_every_row
 from tree_speculative_verification_gb300 import api
 from tree_speculative_verification_gb300.step import DeviceStep
 
@@ -39,7 +38,8 @@ def test_tq_tile_edges(prefix):
 def test_tq_large_scores_rescale():
     rng = np.random.default_rng(19)
     err, _, _ = _run_case(rng, 1, 2, 128, 100, prefix=[1500], value_scale=3.0)
-    assert err <= 5 * TOL_BF16, err
+    print(f"value scale 3: max-abs error {err:.4f}")
+    assert err <= 3.0 * TOL_BF16, err    # the bound scales with the magnitude of V
 
 
 def test_tq_many_items_ragged():
@@ -58,18 +58,9 @@ def test_tq_request_without_tree():
     assert err <= TOL_BF16, err
 
 
-@pytest.mark.parametrize("name", ["long65b", "opt30b"])
-def test_tq_full_size_sampled(name):
-    w = workload(name)
-    assert api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16) == "k_attn_tq"
-    s = DeviceStep(w)
-    s.build(); s.append(); s.attend()
-    torch.cuda.synchronize()
-    assert s.status.item() == 0
-    parent, tokens, n_nodes, _, _ = oracle_tree(w)
-    rows = sample_rows(w, n_nodes, 48, seed=len(name) + 1)
-    err, _, _ = attention_error(s, w, n_nodes, parent, rows)
-    assert err <= TOL_BF16, err
-    out = s.out.float()
-    for b in range(w.B):
-        assert torch.isfinite(out[b, : int(n_nodes[b])]).all()
+@pytest.mark.parametrize("name", ["llama7b", "merge"])
+def test_tq_full_size_every_row_small_trees(name):
+    """The persistent kernel forced onto the 21-node and merged-chain layers:
+    256 and 512 items on 152 CTAs (most CTAs take several items from the
+    queue), ragged prefixes U[512, 4096]; every output row checked."""
+    full_size_every_row(name, "k_attn_tq")

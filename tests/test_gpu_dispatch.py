@@ -1,8 +1,8 @@
 """Longest-first dispatch of the attention CTAs (grid row r takes the request
 with the r-th largest key count): only the order in which (request, head)
 pairs are scheduled changes, so the output must be bit-identical to request
-order, with and without key splits; the tcgen05 kernels keep request order
-and must not depend on the switch."""
+order, with and without key splits; the persistent tcgen05 kernel takes its
+items from a queue and must not depend on the switch."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +22,7 @@ def _attend(w, monkeypatch, lpt):
     return s.out.view(torch.int16).cpu().numpy()
 
 
-@pytest.mark.parametrize("kernel,splits", [("mma", ""), ("mma", "3"), ("tc", ""), ("tc", "2")])
+@pytest.mark.parametrize("kernel,splits", [("mma", ""), ("mma", "3"), ("tq", "")])
 def test_longest_first_is_bit_identical(kernel, splits, monkeypatch):
     """Merge-based trees over ragged prefixes U[512, 4096] (batch 16)."""
     monkeypatch.setenv("TREESPEC_ATTN_KERNEL", kernel)

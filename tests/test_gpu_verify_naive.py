@@ -11,7 +11,7 @@ import oracle
 from tree_speculative_verification_gb300 import api
 from tree_speculative_verification_gb300.step import to_device
 
-from _helpers import oracle_tree, workload
+from _helpers import exclusion_bound, low_margin_prob, oracle_tree, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -48,31 +48,48 @@ def _run(logits_nodes, par, tok, n_nodes, uni, T, p_row=None, logits_rows=None):
     op = torch.full((B, n_max + 1), -1, dtype=torch.int32, device="cuda")
     oc = torch.zeros(B, dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lm = torch.full((B,), -1, dtype=torch.int32, device="cuda")
     rows = logits_nodes if logits_rows is None else logits_rows
-    api.verify_naive(ot, op, oc, d(rows), d(uni), T, t, p_row=None if p_row is None else d(p_row), status=st)
+    api.verify_naive(ot, op, oc, d(rows), d(uni), T, t, p_row=None if p_row is None else d(p_row), status=st,
+                     lowmargin=lm)
     torch.cuda.synchronize()
-    return ot.cpu().numpy(), op.cpu().numpy(), oc.cpu().numpy(), int(st.item())
+    return ot.cpu().numpy(), op.cpu().numpy(), oc.cpu().numpy(), int(st.item()), lm.cpu().numpy()
 
 
-def _compare(logits_nodes, par, tok, n_nodes, uni, T, got, max_excluded):
-    ot, op, oc, _ = got
+def _compare(logits_nodes, par, tok, n_nodes, uni, T, got):
+    """Bit-exact up to the first low-margin draw on the oracle's path; every
+    request that differs at all must carry a device low-margin count; the
+    number of requests with an oracle low-margin draw is bounded by the
+    expected number (the measure of u near a cumulative-sum boundary, summed
+    over the nodes of each oracle path) plus four standard deviations."""
+    ot, op, oc, _, lowm = got
     ref = oracle.verify_naive(logits_nodes, par, tok, n_nodes, uni, T)
-    excluded = 0
+    excluded, probs = 0, []
     for b in range(par.shape[0]):
         n = int(n_nodes[b])
         rc = int(ref["count"][b])
         lm = _low_margin_pos(logits_nodes[b], par[b], tok[b], n, uni[b, 1], T, ref["tokens"][b], rc)
+        path = [int(np.nonzero(par[b, :n] == -1)[0][0])]    # the oracle's path: first child holding each token
+        for x in ref["tokens"][b, :rc - 1]:
+            path.append([v for v in _children(par[b], path[-1], n) if tok[b, v] == x][0])
+        probs.append(min(1.0, sum(low_margin_prob(logits_nodes[b, u], T) for u in path)))
         k = min(lm, rc)
         assert ot[b, :k].tolist() == ref["tokens"][b, :k].tolist(), b
         if lm >= rc:
             assert oc[b] == rc, b
         else:
             excluded += 1
+        same = oc[b] == rc and ot[b, :rc].tolist() == ref["tokens"][b, :rc].tolist()
+        assert same or lowm[b] > 0, f"request {b} differs from the oracle with no low-margin draw reported"
+        assert lowm[b] >= 0
         # the path: op[0] is the root, op[i + 1] a child of op[i] whose token is ot[i]
         assert par[b, op[b, 0]] == -1
         for i in range(int(oc[b]) - 1):
             assert par[b, op[b, i + 1]] == op[b, i] and tok[b, op[b, i + 1]] == ot[b, i]
-    assert excluded <= max_excluded, excluded
+    bound = exclusion_bound(probs)
+    print(f"naive: requests with an oracle low-margin draw {excluded} of {par.shape[0]} (bound {bound:.1f}); "
+          f"device-reported {int((lowm > 0).sum())}")
+    assert excluded <= bound, (excluded, bound)
     return ref
 
 
@@ -101,8 +118,7 @@ def test_naive_random_trees(V, T):
     nn = np.full(B, n, np.int32)
     # with 32000 entries the drawn token itself often holds under 1e-6 of the mass,
     # which puts both of its cumulative-sum boundaries inside the margin
-    ref = _compare(logits, par, tok, nn, uni, T, _run(logits, par, tok, nn, uni, T),
-                   max_excluded=3 if V < 32000 else B // 5)
+    ref = _compare(logits, par, tok, nn, uni, T, _run(logits, par, tok, nn, uni, T))
     assert ref["count"].max() >= 2   # some walks accept at least one child
 
 
@@ -112,7 +128,7 @@ def test_naive_merge_workload_with_row_map():
     parent, tokens, n_nodes, p_row, _ = oracle_tree(w)
     logits_nodes = np.stack([w.logits[b][p_row[b]] for b in range(w.B)])   # the oracle reads one row per node
     got = _run(logits_nodes, parent, tokens, n_nodes, w.uniforms, w.temperature, p_row=p_row, logits_rows=w.logits)
-    _compare(logits_nodes, parent, tokens, n_nodes, w.uniforms, w.temperature, got, max_excluded=1)
+    _compare(logits_nodes, parent, tokens, n_nodes, w.uniforms, w.temperature, got)
 
 
 def test_naive_nonfinite_row_empties_the_request():
@@ -123,7 +139,7 @@ def test_naive_nonfinite_row_empties_the_request():
     logits[1, 0, 7] = np.inf                 # request 1's root row: the walk reads it first
     tok = rng.integers(0, V, (B, n)).astype(np.int32)
     uni = rng.random((B, 2, n)).astype(np.float32)
-    ot, op, oc, st = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
+    ot, op, oc, st, _ = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
     assert oc[1] == 0 and oc[0] >= 1 and oc[2] >= 1
     assert st & api.STATUS_NONFINITE
 
@@ -144,7 +160,7 @@ def test_mss_accepts_at_least_as_many_tokens_as_naive():
             cdf = np.cumsum(q[b, par[b, v]].astype(np.float64))
             tok[b, v] = min(int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right")), V - 1)
     uni = rng.random((B, 2, n)).astype(np.float32)
-    _, _, naive_counts, _ = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
+    _, _, naive_counts, _, _ = _run(logits, par, tok, np.full(B, n, np.int32), uni, 1.0)
     t = api.Tree(B, n)
     d = lambda a: to_device(a, "cuda")
     api.tree_build(t, d(tok), d(par), d(np.full(B, n, np.int32)))

@@ -69,8 +69,8 @@ def load_library(path: str | None = None):
         "tree_build_append": [T, P, P, I, P, P, P, P, P, I, I, I, I, P, P],
         "tree_attention": [P, P, P, P, P, T, I, I, I, I, F, P, Z, P, P],
         "verify_greedy": [P, P, P, P, P, T, I, P, Z, P, P],
-        "verify_mss": [P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
-        "verify_naive": [P, P, P, P, P, I, P, F, T, I, P, P],
+        "verify_mss": [P, P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
+        "verify_naive": [P, P, P, P, P, P, I, P, F, T, I, P, P],
         "tree_expand_topk": [P, P, P, I, I, I, P, I, I, P, P],
         "kv_append_paged": [C.POINTER(ts_paged_kv), P, P, P, T, I, I, P, P],
         "tree_attention_paged": [P, P, C.POINTER(ts_paged_kv), P, T, I, I, F, P, Z, P, P],
@@ -249,20 +249,24 @@ def verify_greedy(out_tokens, out_path, out_count, logits, tree: Tree, argmax_ou
 
 
 def verify_mss(out_tokens, out_path, out_count, target_logits, ssm_probs, q_row, uniforms, temperature, tree: Tree,
-               p_row=None, status=None, stream=None):
+               p_row=None, status=None, stream=None, lowmargin=None):
+    """lowmargin: optional int32 [B], the number of decisions per request taken
+    with a margin below 1e-6."""
     lib = load_library()
     NP, V = target_logits.shape[1], target_logits.shape[2]
     NQ = ssm_probs.shape[1]
-    _check(lib.verify_mss(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(target_logits),
+    _check(lib.verify_mss(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(_i32(lowmargin, "lowmargin")),
+                          _ptr(target_logits),
                           _ptr(_i32(p_row, "p_row")), NP, _ptr(ssm_probs), _ptr(_i32(q_row, "q_row")), NQ,
                           _ptr(uniforms), float(temperature), tree.c, V, _ptr(status), _stream(stream)), "verify_mss")
 
 
 def verify_naive(out_tokens, out_path, out_count, target_logits, uniforms, temperature, tree: Tree, p_row=None,
-                 status=None, stream=None):
+                 status=None, stream=None, lowmargin=None):
     lib = load_library()
     NP, V = target_logits.shape[1], target_logits.shape[2]
-    _check(lib.verify_naive(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(target_logits),
+    _check(lib.verify_naive(_ptr(out_tokens), _ptr(out_path), _ptr(out_count), _ptr(_i32(lowmargin, "lowmargin")),
+                            _ptr(target_logits),
                             _ptr(_i32(p_row, "p_row")), NP, _ptr(uniforms), float(temperature), tree.c, V,
                             _ptr(status), _stream(stream)), "verify_naive")
 

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtreespec.so")
-SOURCES = ["api.cu", "tree_build.cu", "kv.cu", "attn_f32.cu", "attn_bf16.cu", "attn_kt.cu", "attn_tq.cu", "verify.cu", "attn_noalloc.cu"]
+SOURCES = ["api.cu", "tree_build.cu", "kv.cu", "attn_f32.cu", "attn_bf16.cu", "attn_tq.cu", "verify.cu", "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -67,6 +67,20 @@ ts_status set_error(ts_status st, const char *fmt, ...) {
 }  // namespace ts
 
 namespace ts {
+// The host checks of tree_attention (tree, shape, NULL pointers, alignment),
+// shared with tree_attention_noalloc so that both reject before enqueuing anything.
+ts_status check_attention_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max, ts_dtype dtype,
+                               const char *who) {
+    ts_status st = check_tree(t, who);
+    if (st) return st;
+    if ((st = check_attn_shape(who, t, H, d, L_max, dtype))) return st;
+    if (!out || !q || !k_cache || !v_cache || !prefix_len) return fail(TS_ERR_INVALID_ARG, "%s: NULL pointer", who);
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(TS_ERR_INVALID_ARG, "%s: q, out and caches must be 16-byte aligned", who);
+    return TS_OK;
+}
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char *e = getenv("TREESPEC_PDL");
@@ -200,13 +214,9 @@ ts_status kv_append(void *k_cache, void *v_cache, const void *k_new, const void 
 ts_status tree_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max, ts_dtype dtype,
                          float scale, void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream) {
-    ts_status st = check_tree(t, "tree_attention");
+    ts_status st = ts::check_attention_args(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype,
+                                            "tree_attention");
     if (st) return st;
-    if ((st = check_attn_shape("tree_attention", t, H, d, L_max, dtype))) return st;
-    if (!out || !q || !k_cache || !v_cache || !prefix_len)
-        return fail(TS_ERR_INVALID_ARG, "tree_attention: NULL pointer");
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-        return fail(TS_ERR_INVALID_ARG, "tree_attention: q, out and caches must be 16-byte aligned");
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     if (dtype == TS_F32)
         return cuda_result(ts::launch_attn_f32((float *)out, (const float *)q, (const float *)k_cache,
@@ -242,10 +252,10 @@ ts_status verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_cou
                        "verify_greedy");
 }
 
-ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *target_logits,
-                     const int32_t *p_row, int NP, const float *ssm_probs, const int32_t *q_row, int NQ,
-                     const float *uniforms, float temperature, const ts_tree *t, int V, uint32_t *status,
-                     cudaStream_t stream) {
+ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                     const float *target_logits, const int32_t *p_row, int NP, const float *ssm_probs,
+                     const int32_t *q_row, int NQ, const float *uniforms, float temperature, const ts_tree *t, int V,
+                     uint32_t *status, cudaStream_t stream) {
     ts_status st = check_tree(t, "verify_mss");
     if (st) return st;
     if (!out_tokens || !out_path || !out_count || !target_logits || !ssm_probs || !q_row || !uniforms)
@@ -258,14 +268,14 @@ ts_status verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
     if (NP < 1) return fail(TS_ERR_INVALID_ARG, "verify_mss: NP=%d must be >= 1", NP);
     if (V % 4 == 0 && !aligned16(target_logits))
         return fail(TS_ERR_INVALID_ARG, "verify_mss: target_logits must be 16-byte aligned");
-    return cuda_result(ts::launch_verify_mss(out_tokens, out_path, out_count, target_logits, p_row, NP, ssm_probs,
-                                             q_row, NQ, uniforms, temperature, *t, V, status, stream),
+    return cuda_result(ts::launch_verify_mss(out_tokens, out_path, out_count, out_lowmargin, target_logits, p_row, NP,
+                                             ssm_probs, q_row, NQ, uniforms, temperature, *t, V, status, stream),
                        "verify_mss");
 }
 
-ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *target_logits,
-                       const int32_t *p_row, int NP, const float *uniforms, float temperature, const ts_tree *t,
-                       int V, uint32_t *status, cudaStream_t stream) {
+ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                       const float *target_logits, const int32_t *p_row, int NP, const float *uniforms,
+                       float temperature, const ts_tree *t, int V, uint32_t *status, cudaStream_t stream) {
     ts_status st = check_tree(t, "verify_naive");
     if (st) return st;
     if (!out_tokens || !out_path || !out_count || !target_logits || !uniforms)
@@ -277,8 +287,8 @@ ts_status verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_coun
     if (NP < 1) return fail(TS_ERR_INVALID_ARG, "verify_naive: NP=%d must be >= 1", NP);
     if (V % 4 == 0 && !aligned16(target_logits))
         return fail(TS_ERR_INVALID_ARG, "verify_naive: target_logits must be 16-byte aligned");
-    return cuda_result(ts::launch_verify_naive(out_tokens, out_path, out_count, target_logits, p_row, NP, uniforms,
-                                               temperature, *t, V, status, stream),
+    return cuda_result(ts::launch_verify_naive(out_tokens, out_path, out_count, out_lowmargin, target_logits, p_row,
+                                               NP, uniforms, temperature, *t, V, status, stream),
                        "verify_naive");
 }
 
@@ -341,7 +351,7 @@ ts_status tree_attention_paged(void *out, const void *q, const ts_paged_kv *kv, 
         return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: q and out must be 16-byte aligned");
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
     const int L_max = kv->max_pages * TS_PAGE_KEYS;
-    const ts::AttnPlan plan = ts::attn_plan(t->B, H, t->n_max, d, L_max, TS_BF16, false);
+    const ts::AttnPlan plan = ts::attn_plan(t->B, H, t->n_max, d, L_max, TS_BF16);
     if (!ws || ws_bytes < plan.ws_bytes)
         return fail(TS_ERR_INVALID_ARG, "tree_attention_paged: workspace of %zu bytes needed, %zu given",
                     plan.ws_bytes, ws ? ws_bytes : (size_t)0);

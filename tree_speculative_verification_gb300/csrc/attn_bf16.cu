@@ -563,793 +563,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
 }
 
 
-// ============================================================================
-// tcgen05 variant (trees of up to 128 nodes, head_dim 128).
-//
-// One CTA of 10 warps per (request, head, key chunk):
-//   warp 0    TMA producer (lane 0) and TMEM owner (alloc / dealloc)
-//   warp 1    MMA issuer (lane 0): S = Q K^T and O += P V with tcgen05.mma
-//   warps 2-5 softmax stream 0 (even key tiles), warps 6-9 stream 1 (odd
-//             tiles): thread r of TMEM lane quarter (warp % 4) owns node row
-//             r, reads its score row from the stream's TMEM S buffer, masks
-//             it, keeps a running max (rescaling the stream's O in TMEM only
-//             when the max grows by more than 2^8), writes bf16 P to the
-//             stream's shared-memory P buffer.
-// The two streams have their own S (64 columns) and O (128 columns) in TMEM,
-// so the tensor core works on one stream while the other's softmax runs; at
-// the end the two (max, sum, O) partials are merged by log-sum-exp.
-// Per 64-key tile: S (M = 128 node rows, N = 64 keys, K = 128) and
-// O += P V (M = 128, N = 128, K = 64 keys). Q, K and P are K-major, V is
-// MN-major, all in the 128-byte swizzled layout TMA writes. Every wait is
-// bounded; TMEM is freed on every exit path.
-// ============================================================================
-struct TcCfg {
-    static constexpr int D = 128, TKT = 64, STAGES = 6, NODES = 128, STREAMS = 2;
-    static constexpr int THREADS = 64 + STREAMS * 128;
-    static constexpr int BOX_BYTES = TKT * 128;           // 64 key rows x 128 bytes
-    static constexpr int TILE_BYTES = 2 * BOX_BYTES;      // K (or V) of 64 keys x 128 dims
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K then V
-    static constexpr int ANC_WORDS = 4;                   // 128 nodes
-    static constexpr int OFF_ANC = STAGES * STAGE_BYTES;
-    static constexpr int OFF_PERM = OFF_ANC + NODES * ANC_WORDS * 4;
-    static constexpr int OFF_ML = OFF_PERM + NODES * 4;   // stream 1's (max, sum) per row for the merge
-    static constexpr int NBAR = 2 * STAGES + 4 * STREAMS + 2;
-    static constexpr int OFF_BAR = OFF_ML + NODES * 8;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    // TMEM columns: S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384), Q [384,448)
-    // (bf16 pairs), P0 [448,480) P1 [480,512) (bf16 pairs)
-    static constexpr uint32_t TMEM_COLS = 512, Q_COL = 384, P_COL = 448;
-};
-
-__global__ void __launch_bounds__(TcCfg::THREADS, 1) k_attn_tc(const __grid_constant__ CUtensorMap map_k,
-                                                               const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
-    using C = TcCfg;
-    constexpr int D = C::D;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const uint32_t sm_base = smem_u32(sm);
-    uint32_t *anc_s = (uint32_t *)(sm + C::OFF_ANC);
-    int *perm_s = (int *)(sm + C::OFF_PERM);
-    float2 *ml_s = (float2 *)(sm + C::OFF_ML);
-    volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout, [2] merge flag
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.y, h = blockIdx.x, sidx = blockIdx.z;
-    const ts_tree &t = a.t;
-    pdl_wait();
-    pdl_trigger();
-    const int n = t.n_nodes[b], P = a.prefix_len[b];
-    if (n <= 0) return;
-    if (P < 0 || P + n > a.L_max) {
-        if (sidx == 0 && h == 0 && tid == 0) flag(a.status, TS_STATUS_INDEX);
-        return;
-    }
-    const int L = P + n;
-    const int chunk_keys = a.chunk_tiles * TK;   // the plan counts 64-key tiles
-    const int S_b = (L + chunk_keys - 1) / chunk_keys;
-    if (sidx >= S_b) return;
-    const int k_begin = sidx * chunk_keys, k_end = min(L, k_begin + chunk_keys);
-    const int ntiles = (k_end - k_begin + C::TKT - 1) / C::TKT;
-
-    const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
-    const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
-    const uint32_t pfull = sfree + 8 * C::STREAMS, pvdone = pfull + 8 * C::STREAMS;
-    const uint32_t fin = pvdone + 8 * C::STREAMS, qready = fin + 8;
-
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (tid == 32) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, 1);
-        }
-        for (int x = 0; x < C::STREAMS; ++x) {
-            mbar_init(sfull + 8 * x, 1);
-            mbar_init(sfree + 8 * x, 4);
-            mbar_init(pfull + 8 * x, 4);
-            mbar_init(pvdone + 8 * x, 1);
-        }
-        mbar_init(fin, 1);
-        mbar_init(qready, 4);
-        misc[1] = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    const int n_max = t.n_max, W = TS_MASK_WORDS(n_max);
-    for (int r = tid; r < C::NODES; r += C::THREADS) perm_s[r] = r < n ? t.perm[(size_t)b * n_max + r] : -1;
-    for (int idx = tid; idx < C::NODES * C::ANC_WORDS; idx += C::THREADS) {
-        const int r = idx / C::ANC_WORDS, w = idx % C::ANC_WORDS;
-        anc_s[idx] = (r < n && w < W) ? t.anc[((size_t)b * n_max + r) * W + w] : 0u;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = (uint32_t)misc[0];
-    if (warp >= 2 && warp < 6) {
-        // Q rows (DFS order) into TMEM as the S MMA's A operand: lane = node row,
-        // column c = dims 2c, 2c+1; zero rows past n. Stream 0's four warps
-        // cover the four lane quarters.
-        const int row = (warp & 3) * 32 + lane;
-        const uint4 *src = row < n ? (const uint4 *)(a.q + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D) : nullptr;
-        const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16) + C::Q_COL;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t qw[32];
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                const uint4 v = src ? __ldg(src + half * 8 + c4) : make_uint4(0u, 0u, 0u, 0u);
-                qw[4 * c4] = v.x;
-                qw[4 * c4 + 1] = v.y;
-                qw[4 * c4 + 2] = v.z;
-                qw[4 * c4 + 3] = v.w;
-            }
-            tc_st32u(tq + half * 32, qw);
-        }
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(qready);
-    }
-
-    if (warp == 0) {
-        if (lane == 0) {   // ---------------------------------------------- TMA producer
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j % C::STAGES;
-                const int row = tile_row(a, b, h, k_begin + j * C::TKT);   // fetched before the wait
-                if (j >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((j / C::STAGES) - 1) & 1u)) {
-                    misc[1] = 1;
-                    break;
-                }
-                const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
-                mbar_expect_tx(full + 8 * st, C::STAGE_BYTES);
-#pragma unroll
-                for (int bx = 0; bx < 2; ++bx) {
-                    tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, full + 8 * st);
-                    tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, full + 8 * st);
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {   // ---------------------------------------------- MMA issuer
-            constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
-            // S of tile j into stream (j & 1)'s score buffer
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % C::STAGES, x = j & 1, k = j >> 1;
-                if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) return false;
-                if (k >= 1 && !mbar_wait_bounded(sfree + 8 * x, (uint32_t)(k - 1) & 1u)) return false;
-                tc_fence_after();
-                const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    tc_mma_ts(tmem + x * C::TKT, tmem + C::Q_COL + kk * 8, bd, idesc_s, kk > 0);
-                }
-                tc_commit(sfull + 8 * x);
-                return true;
-            };
-            bool ok = mbar_wait_bounded(qready, 0);   // Q is in TMEM
-            tc_fence_after();
-            ok = ok && issue_s(0);
-            for (int j = 0; j < ntiles && ok; ++j) {
-                if (j + 1 < ntiles && !(ok = issue_s(j + 1))) break;
-                const int x = j & 1, k = j >> 1, st = j % C::STAGES;
-                if (!mbar_wait_bounded(pfull + 8 * x, (uint32_t)k & 1u)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t vbase = sm_base + st * C::STAGE_BYTES + C::TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < C::TKT / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
-                    tc_mma_ts(tmem + 2 * C::TKT + x * D, tmem + C::P_COL + x * 32 + kk * 8, bd, idesc_pv,
-                              (k > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(empty + 8 * st);
-                tc_commit(pvdone + 8 * x);
-            }
-            if (!ok) misc[1] = 1;
-            tc_commit(fin);   // completes once every MMA issued above has finished
-            if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
-        }
-        __syncwarp();
-    } else {   // --------------------------------------------------------- softmax
-        const int x = (warp - 2) >> 2;                      // stream
-        const int wq = warp & 3, row = wq * 32 + lane;       // TMEM lane quarter, node row
-        const bool active = wq * 32 < n;
-        const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t s_col = x * C::TKT, o_col = 2 * C::TKT + x * D;
-        uint32_t aw[C::ANC_WORDS];
-#pragma unroll
-        for (int w = 0; w < C::ANC_WORDS; ++w) aw[w] = anc_s[row * C::ANC_WORDS + w];
-        const float c = a.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        int k = 0;
-        for (int j = x; j < ntiles && ok; j += 2, ++k) {
-            if (!mbar_wait_warp(sfull + 8 * x, (uint32_t)k & 1u)) { ok = false; break; }
-            tc_fence_after();
-            float sv[64];
-            if (active) {
-                tc_ld32(tl + s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
-                tc_ld32(tl + s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-                tc_wait_ld();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sfree + 8 * x);
-            const int key_base = k_begin + j * C::TKT;
-            // this stream's previous PV must be done before its O is rescaled or
-            // its P buffer rewritten
-            if (k >= 1 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(k - 1) & 1u)) { ok = false; break; }
-            uint32_t pk[32];
-            if (active) {
-                if (key_base + C::TKT > P || key_base + C::TKT > k_end) {
-#pragma unroll
-                    for (int e = 0; e < C::TKT; ++e) {
-                        const int key = key_base + e;
-                        bool vis = key < k_end;
-                        if (vis && key >= P) {
-                            const int tk = key - P;
-                            vis = (aw[tk >> 5] >> (tk & 31)) & 1u;
-                        }
-                        if (!vis) sv[e] = -INFINITY;
-                    }
-                }
-                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};   // four independent chains
-#pragma unroll
-                for (int e = 4; e < C::TKT; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
-                const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
-                float alpha = 1.f;
-                bool resc = false;
-                if (m_run == -INFINITY) {
-                    m_run = mt;                              // nothing accumulated yet for this row
-                } else if (mt > m_run + 8.f) {
-                    alpha = exp2f(m_run - mt);
-                    m_run = mt;
-                    resc = true;
-                }
-                if (__any_sync(0xffffffffu, resc)) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        float o[32];
-                        tc_ld32(tl + o_col + q4 * 32, o);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tc_st32(tl + o_col + q4 * 32, o);
-                    }
-                    tc_wait_st();
-                    l_run *= alpha;
-                }
-                const float mu = m_run == -INFINITY ? 0.f : m_run;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < C::TKT; e += 2) {
-                    float r0, r1;
-                    pk[e >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[e], c, -mu)), exp2f(__fmaf_rn(sv[e + 1], c, -mu)), r0, r1);
-                    ls[(e >> 1) & 3] += r0 + r1;
-                }
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            }
-            if (key_base + C::TKT > k_end) {
-                // last tile: V rows past the chunk may hold anything (even NaN);
-                // zero them before the PV reads the stage, so 0 * V stays 0
-                const int st = j % C::STAGES;
-                if (!mbar_wait_warp(full + 8 * st, (uint32_t)(j / C::STAGES) & 1u)) { ok = false; break; }
-                unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
-                const int r0 = k_end - key_base;
-                for (int idx = tid - 64 - 128 * x; idx < (C::TKT - r0) * 16; idx += 128) {
-                    const int r = r0 + (idx >> 4), c16 = idx & 15;
-                    *(uint4 *)(vt + (c16 >> 3) * C::BOX_BYTES + r * 128 + ((c16 & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_async_smem();
-            }
-            if (active) {   // P (bf16 pairs) into this stream's TMEM columns: the PV MMA's A operand
-                tc_st32u(tl + C::P_COL + x * 32, pk);
-                tc_wait_st();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pfull + 8 * x);
-        }
-        // this stream's O is complete once its last PV has finished
-        const int nk = (ntiles - x + 1) / 2;                 // tiles this stream processed
-        if (ok && nk > 0 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(nk - 1) & 1u)) ok = false;
-        if (!ok) misc[1] = 1;
-        tc_fence_after();
-        if (x == 1) ml_s[row] = make_float2(nk > 0 ? m_run : -INFINITY, nk > 0 ? l_run : 0.f);
-        asm volatile("bar.sync 1, %0;" ::"n"(C::STREAMS * 128) : "memory");   // the softmax warps only
-        const int stop = __any_sync(0xffffffffu, misc[1]);   // one verdict per warp
-        if (x == 0 && active && !stop) {
-            // merge the two streams by log-sum-exp, then write the row
-            const float2 m1 = ml_s[row];
-            const float M = fmaxf(m_run, m1.x);
-            const float f0 = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
-            const float f1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
-            const float lsum = l_run * f0 + m1.y * f1;
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const size_t ps = ((size_t)b * a.H + h) * a.splits + sidx;
-            if (row < n && S_b > 1) {
-                a.part_ml[ps * 2 * a.n_pad + row] = M;
-                a.part_ml[ps * 2 * a.n_pad + a.n_pad + row] = lsum;
-            }
-            uint4 *dst = row < n && S_b == 1 ? (uint4 *)(a.out + (((size_t)b * n_max + perm_s[row]) * a.H + h) * D)
-                                             : nullptr;
-            float4 *po = row < n && S_b > 1 ? (float4 *)(a.part_o + (ps * a.n_pad + row) * D) : nullptr;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
-                float o[32];
-                tc_ld32(tl + 2 * C::TKT + q4 * 32, o);
-                tc_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] *= f0;
-                if (ntiles >= 2) {   // stream 1 wrote O1 (rows it never saw hold zeros there); CTA-uniform
-                    float o1[32];
-                    tc_ld32(tl + 2 * C::TKT + D + q4 * 32, o1);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __fmaf_rn(o1[e], f1, o[e]);
-                }
-                if (dst) {
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float d0, d1;
-                        uint4 v;
-                        v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
-                        v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
-                        v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
-                        v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
-                        dst[q4 * 4 + c8] = v;
-                    }
-                } else if (po) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        po[q4 * 8 + c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
-    if (misc[1]) {
-        if (tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
-        return;
-    }
-    if (S_b > 1) merge_splits<D>(a, b, h, n, S_b, perm_s, (int *)misc + 2, C::THREADS);
-}
-
-
-// ============================================================================
-// Persistent tcgen05 variant: the same roles and per-tile work as k_attn_tc,
-// plus warp 10, which loads the next (request, head) item's Q rows, ancestor
-// masks and permutation into a second buffer while the current item streams.
-// Each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...; the K/V stage
-// ring, the TMEM score buffers and the two softmax streams run on across item
-// boundaries, so a new item costs no pipeline refill. Used when no key split
-// is needed (enough (request, head) pairs to fill the GPU).
-// ============================================================================
-struct TpCfg {
-    static constexpr int D = 128, TKT = 64, STAGES = 3, NODES = 128, STREAMS = 2;
-    static constexpr int THREADS = 64 + STREAMS * 128 + 32;
-    static constexpr int LOADER = 2 + 4 * STREAMS;        // warp index of the item loader
-    static constexpr int BOX_BYTES = TKT * 128;
-    static constexpr int TILE_BYTES = 2 * BOX_BYTES;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int QBOX = NODES * 128;
-    static constexpr int Q_BYTES = 2 * QBOX;
-    static constexpr int P_BYTES = NODES * 128;
-    static constexpr int ANC_WORDS = 4;
-    static constexpr int OFF_Q = STAGES * STAGE_BYTES;                 // 2 item buffers
-    static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;                  // one per stream
-    static constexpr int OFF_ANC = OFF_P + STREAMS * P_BYTES;          // 2 item buffers
-    static constexpr int OFF_PERM = OFF_ANC + 2 * NODES * ANC_WORDS * 4;
-    static constexpr int OFF_ML = OFF_PERM + 2 * NODES * 4;           // 2 item buffers of (max, sum)
-    static constexpr int NBAR = 2 * STAGES + 4 * STREAMS + 3 * 2 + 2;  // + q_full, q_free, meta_free, o_free, fin
-    static constexpr int OFF_BAR = OFF_ML + 2 * NODES * 8;
-    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = 512;
-};
-
-// (n, P, L, tiles) of item p = b * H + h; an unusable tree or index error gives 0 tiles.
-struct ItemInfo {
-    int b, h, n, P, L, ntiles;
-};
-
-__device__ __forceinline__ ItemInfo item_info(const AttnArgs &a, int p) {
-    ItemInfo it;
-    it.b = p / a.H;
-    it.h = p - it.b * a.H;
-    it.n = a.t.n_nodes[it.b];
-    it.P = a.prefix_len[it.b];
-    it.L = it.P + it.n;
-    const bool ok = it.n > 0 && it.P >= 0 && it.L <= a.L_max;
-    it.ntiles = ok ? (it.L + TpCfg::TKT - 1) / TpCfg::TKT : 0;
-    return it;
-}
-
-__global__ void __launch_bounds__(TpCfg::THREADS, 1) k_attn_tp(const __grid_constant__ CUtensorMap map_k,
-                                                               const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
-    using C = TpCfg;
-    constexpr int D = C::D;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const uint32_t sm_base = smem_u32(sm);
-    volatile int *misc = (volatile int *)(sm + C::OFF_MISC);   // [0] TMEM base, [1] timeout
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pairs = a.t.B * a.H, G = gridDim.x;
-    const int n_max = a.t.n_max, W = TS_MASK_WORDS(n_max);
-    pdl_wait();
-    pdl_trigger();
-
-    const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
-    const uint32_t sfull = empty + 8 * C::STAGES, sfree = sfull + 8 * C::STREAMS;
-    const uint32_t pfull = sfree + 8 * C::STREAMS, pvdone = pfull + 8 * C::STREAMS;
-    const uint32_t qfull = pvdone + 8 * C::STREAMS, qfree = qfull + 16, metafree = qfree + 16;
-    const uint32_t ofree = metafree + 16, fin = ofree + 8;
-
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (tid == 32) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, 1);
-        }
-        for (int x = 0; x < C::STREAMS; ++x) {
-            mbar_init(sfull + 8 * x, 1);
-            mbar_init(sfree + 8 * x, 4);
-            mbar_init(pfull + 8 * x, 4);
-            mbar_init(pvdone + 8 * x, 1);
-        }
-        for (int q = 0; q < 2; ++q) {
-            mbar_init(qfull + 8 * q, 1);
-            mbar_init(qfree + 8 * q, 1);
-            mbar_init(metafree + 8 * q, 4 * C::STREAMS);
-        }
-        mbar_init(ofree, 4);
-        mbar_init(fin, 1);
-        misc[1] = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = (uint32_t)misc[0];
-
-    if (warp == 0) {
-        if (lane == 0) {   // ---------------------------------------------- TMA producer
-            int g = 0;
-            bool ok = true;
-            for (int p = blockIdx.x; p < pairs && ok; p += G) {
-                const ItemInfo it = item_info(a, p);
-                for (int j = 0; j < it.ntiles; ++j, ++g) {
-                    const int st = g % C::STAGES;
-                    const int row = tile_row(a, p / a.H, p % a.H, j * C::TKT);   // fetched before the wait
-                    if (g >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((g / C::STAGES) - 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
-                    mbar_expect_tx(full + 8 * st, C::STAGE_BYTES);
-#pragma unroll
-                    for (int bx = 0; bx < 2; ++bx) {
-                        tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, full + 8 * st);
-                        tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, full + 8 * st);
-                    }
-                }
-            }
-            if (!ok) misc[1] = 1;
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {   // ---------------------------------------------- MMA issuer
-            constexpr uint32_t idesc_s = idesc_bf16(128, C::TKT, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, D, true);
-            bool ok = true;
-            auto issue_s = [&](int gg, int qb) -> bool {
-                const int st = gg % C::STAGES, x = gg & 1, k = gg >> 1;
-                if (!mbar_wait_bounded(full + 8 * st, (uint32_t)(gg / C::STAGES) & 1u)) return false;
-                if (k >= 1 && !mbar_wait_bounded(sfree + 8 * x, (uint32_t)(k - 1) & 1u)) return false;
-                tc_fence_after();
-                const uint32_t q_base = sm_base + C::OFF_Q + qb * C::Q_BYTES;
-                const uint32_t kbase = sm_base + st * C::STAGE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(q_base + (kk >> 2) * C::QBOX + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(kbase + (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32, 16, 1024);
-                    tc_mma(tmem + x * C::TKT, ad, bd, idesc_s, kk > 0);
-                }
-                tc_commit(sfull + 8 * x);
-                return true;
-            };
-            // PV of tile gg (item-local index j, in the u-th item with tiles); the
-            // first PV of each stream in an item starts O afresh, once the previous
-            // item's O has been read out
-            auto issue_pv = [&](int gg, int j, int u) -> bool {
-                const int x = gg & 1, k = gg >> 1, st = gg % C::STAGES;
-                const bool first = j < 2;
-                if (first && u >= 2 && !mbar_wait_bounded(ofree, (uint32_t)(u - 2) & 1u)) return false;
-                if (!mbar_wait_bounded(pfull + 8 * x, (uint32_t)k & 1u)) return false;
-                tc_fence_after();
-                const uint32_t pbase = sm_base + C::OFF_P + x * C::P_BYTES;
-                const uint32_t vbase = sm_base + st * C::STAGE_BYTES + C::TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < C::TKT / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(pbase + kk * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
-                    tc_mma(tmem + 2 * C::TKT + x * D, ad, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(empty + 8 * st);
-                tc_commit(pvdone + 8 * x);
-                return true;
-            };
-            // S(g + 1) is issued before PV(g), also across item boundaries
-            int g = 0, u = 0, i = 0;
-            int pend_g = -1, pend_j = 0, pend_u = 0;
-            for (int p = blockIdx.x; p < pairs && ok; p += G, ++i) {
-                const ItemInfo it = item_info(a, p);
-                const int qb = i & 1;
-                if (!mbar_wait_bounded(qfull + 8 * qb, (uint32_t)(i >> 1) & 1u)) { ok = false; break; }
-                if (it.ntiles > 0) ++u;
-                for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
-                    if (!issue_s(g, qb)) { ok = false; break; }
-                    if (pend_g >= 0 && !issue_pv(pend_g, pend_j, pend_u)) { ok = false; break; }
-                    pend_g = g;
-                    pend_j = j;
-                    pend_u = u;
-                }
-                tc_commit(qfree + 8 * qb);   // the Q buffer is free once these S MMAs finish
-            }
-            if (ok && pend_g >= 0) ok = issue_pv(pend_g, pend_j, pend_u);
-            if (!ok) misc[1] = 1;
-            tc_commit(fin);
-            if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
-        }
-        __syncwarp();
-    } else if (warp == C::LOADER) {   // --------------------------------------- item loader
-        bool ok = true;
-        int i = 0;
-        for (int p = blockIdx.x; p < pairs; p += G, ++i) {
-            const int qb = i & 1;
-            if (ok && i >= 2) {
-                ok = mbar_wait_warp(qfree + 8 * qb, (uint32_t)((i >> 1) - 1) & 1u) &&
-                     mbar_wait_warp(metafree + 8 * qb, (uint32_t)((i >> 1) - 1) & 1u);
-                if (!ok) misc[1] = 1;
-            }
-            const ItemInfo it = item_info(a, p);
-            if (ok && it.ntiles > 0) {
-                int *perm_s = (int *)(sm + C::OFF_PERM) + qb * C::NODES;
-                uint32_t *anc_s = (uint32_t *)(sm + C::OFF_ANC) + qb * C::NODES * C::ANC_WORDS;
-                unsigned char *qs = sm + C::OFF_Q + qb * C::Q_BYTES;
-                for (int r = lane; r < C::NODES; r += 32) perm_s[r] = r < it.n ? a.t.perm[(size_t)it.b * n_max + r] : -1;
-                for (int idx = lane; idx < C::NODES * C::ANC_WORDS; idx += 32) {
-                    const int r = idx / C::ANC_WORDS, w = idx % C::ANC_WORDS;
-                    anc_s[idx] = (r < it.n && w < W) ? a.t.anc[((size_t)it.b * n_max + r) * W + w] : 0u;
-                }
-                __syncwarp();
-                // the item's Q rows, 128-byte swizzled K-major, eight loads in flight per lane
-                for (int base = lane; base < C::NODES * 16; base += 8 * 32) {
-                    uint4 qv[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int idx = base + k * 32, r = idx >> 4, c = idx & 15;
-                        qv[k] = make_uint4(0u, 0u, 0u, 0u);
-                        if (idx < C::NODES * 16 && r < it.n)
-                            qv[k] = __ldg((const uint4 *)(a.q + (((size_t)it.b * n_max + perm_s[r]) * a.H + it.h) * D) + c);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int idx = base + k * 32, r = idx >> 4, c = idx & 15;
-                        if (idx < C::NODES * 16)
-                            *(uint4 *)(qs + (c >> 3) * C::QBOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = qv[k];
-                    }
-                }
-                fence_async_smem();
-            } else if (it.n > 0 && it.ntiles == 0 && lane == 0 && it.h == 0) {
-                flag(a.status, TS_STATUS_INDEX);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qfull + 8 * qb);
-        }
-    } else {   // --------------------------------------------------------- softmax
-        const int x = (warp - 2) >> 2;                      // stream
-        const int wq = warp & 3, row = wq * 32 + lane;       // TMEM lane quarter, node row
-        const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t s_col = x * C::TKT, o_col = 2 * C::TKT + x * D;
-        const float c = a.scale_log2;
-        bool ok = true;
-        int g = 0, kx = 0, i = 0;
-        for (int p = blockIdx.x; p < pairs; p += G, ++i) {
-            const int qb = i & 1;
-            if (ok && !mbar_wait_warp(qfull + 8 * qb, (uint32_t)(i >> 1) & 1u)) { ok = false; misc[1] = 1; }
-            const ItemInfo it = item_info(a, p);
-            if (it.ntiles > 0) {
-                const bool active = wq * 32 < it.n;
-                const uint32_t *anc_s = (const uint32_t *)(sm + C::OFF_ANC) + qb * C::NODES * C::ANC_WORDS;
-                uint32_t aw[C::ANC_WORDS];
-#pragma unroll
-                for (int w = 0; w < C::ANC_WORDS; ++w) aw[w] = anc_s[row * C::ANC_WORDS + w];
-                const int g0 = g;
-                const int n_even = ((g0 + it.ntiles + 1) >> 1) - ((g0 + 1) >> 1);
-                const int nk_mine = x == 0 ? n_even : it.ntiles - n_even;
-                const int nk_other = it.ntiles - nk_mine;
-                float m_run = -INFINITY, l_run = 0.f;
-                for (int j = 0; j < it.ntiles; ++j, ++g) {
-                    if ((g & 1) != x || !ok) continue;
-                    const int k = kx++;
-                    if (!mbar_wait_warp(sfull + 8 * x, (uint32_t)k & 1u)) { ok = false; continue; }
-                    tc_fence_after();
-                    float sv[64];
-                    if (active) {
-                        tc_ld32(tl + s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
-                        tc_ld32(tl + s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-                        tc_wait_ld();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(sfree + 8 * x);
-                    const int key_base = j * C::TKT;
-                    if (k >= 1 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(k - 1) & 1u)) { ok = false; continue; }
-                    uint32_t pk[32];
-                    if (active) {
-                        if (key_base + C::TKT > it.P) {
-#pragma unroll
-                            for (int e = 0; e < C::TKT; ++e) {
-                                const int key = key_base + e;
-                                bool vis = key < it.L;
-                                if (vis && key >= it.P) {
-                                    const int tk = key - it.P;
-                                    vis = (aw[tk >> 5] >> (tk & 31)) & 1u;
-                                }
-                                if (!vis) sv[e] = -INFINITY;
-                            }
-                        }
-                        float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-                        for (int e = 4; e < C::TKT; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], sv[e]);
-                        const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
-                        float alpha = 1.f;
-                        bool resc = false;
-                        if (m_run == -INFINITY) {
-                            m_run = mt;
-                        } else if (mt > m_run + 8.f) {
-                            alpha = exp2f(m_run - mt);
-                            m_run = mt;
-                            resc = true;
-                        }
-                        if (__any_sync(0xffffffffu, resc)) {
-                            tc_fence_after();
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                float o[32];
-                                tc_ld32(tl + o_col + q4 * 32, o);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                                tc_st32(tl + o_col + q4 * 32, o);
-                            }
-                            tc_wait_st();
-                            l_run *= alpha;
-                        }
-                        const float mu = m_run == -INFINITY ? 0.f : m_run;
-                        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int e = 0; e < C::TKT; e += 2) {
-                            float r0, r1;
-                            pk[e >> 1] = pack_bf16(exp2f(__fmaf_rn(sv[e], c, -mu)), exp2f(__fmaf_rn(sv[e + 1], c, -mu)),
-                                                   r0, r1);
-                            ls[(e >> 1) & 3] += r0 + r1;
-                        }
-                        l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    }
-                    if (key_base + C::TKT > it.L) {
-                        // last tile of the item: zero the V rows past its keys (they may hold anything)
-                        const int st = g % C::STAGES;
-                        if (!mbar_wait_warp(full + 8 * st, (uint32_t)(g / C::STAGES) & 1u)) { ok = false; continue; }
-                        unsigned char *vt = sm + st * C::STAGE_BYTES + C::TILE_BYTES;
-                        const int r0 = it.L - key_base;
-                        for (int idx = tid - 64 - 128 * x; idx < (C::TKT - r0) * 16; idx += 128) {
-                            const int r = r0 + (idx >> 4), c16 = idx & 15;
-                            *(uint4 *)(vt + (c16 >> 3) * C::BOX_BYTES + r * 128 + ((c16 & 7) << 4)) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_async_smem();
-                    }
-                    if (active) {
-                        unsigned char *prow = sm + C::OFF_P + x * C::P_BYTES + row * 128;
-#pragma unroll
-                        for (int c16 = 0; c16 < 8; ++c16)
-                            *(uint4 *)(prow + ((c16 ^ (row & 7)) << 4)) =
-                                make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-                        fence_async_smem();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(pfull + 8 * x);
-                }
-                // this stream's O holds the item once its last PV has finished
-                if (ok && nk_mine > 0 && !mbar_wait_warp(pvdone + 8 * x, (uint32_t)(kx - 1) & 1u)) ok = false;
-                if (!ok) misc[1] = 1;
-                tc_fence_after();
-                float2 *ml_s = (float2 *)(sm + C::OFF_ML) + qb * C::NODES;
-                if (x == 1) ml_s[row] = make_float2(nk_mine > 0 ? m_run : -INFINITY, nk_mine > 0 ? l_run : 0.f);
-                asm volatile("bar.sync 1, %0;" ::"n"(C::STREAMS * 128) : "memory");   // softmax warps, every item
-                const int stop = __any_sync(0xffffffffu, misc[1]);
-                if (x == 0) {
-                    if (active && !stop) {
-                        const float2 m1 = ml_s[row];
-                        const float m0 = nk_mine > 0 ? m_run : -INFINITY;
-                        const float M = fmaxf(m0, m1.x);
-                        const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
-                        const float f1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
-                        const float lsum = (nk_mine > 0 ? l_run : 0.f) * f0 + m1.y * f1;
-                        const int *perm_s = (const int *)(sm + C::OFF_PERM) + qb * C::NODES;
-                        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                        uint4 *dst = row < it.n ? (uint4 *)(a.out + (((size_t)it.b * n_max + perm_s[row]) * a.H + it.h) * D)
-                                                : nullptr;
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {   // 32 columns at a time
-                            float o[32];
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = 0.f;
-                            if (nk_mine > 0) {     // uniform: stream 0's O holds this item
-                                float o0[32];
-                                tc_ld32(tl + 2 * C::TKT + q4 * 32, o0);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) o[e] = o0[e] * f0;
-                            }
-                            if (nk_other > 0) {    // uniform: stream 1's O holds this item
-                                float o1[32];
-                                tc_ld32(tl + 2 * C::TKT + D + q4 * 32, o1);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) o[e] = __fmaf_rn(o1[e], f1, o[e]);
-                            }
-                            if (dst) {
-#pragma unroll
-                                for (int c8 = 0; c8 < 4; ++c8) {
-                                    float d0, d1;
-                                    uint4 v;
-                                    v.x = pack_bf16(o[8 * c8] * inv, o[8 * c8 + 1] * inv, d0, d1);
-                                    v.y = pack_bf16(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv, d0, d1);
-                                    v.z = pack_bf16(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv, d0, d1);
-                                    v.w = pack_bf16(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv, d0, d1);
-                                    dst[q4 * 4 + c8] = v;
-                                }
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(ofree);   // both streams' O may be overwritten now
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(metafree + 8 * qb);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
-    if (misc[1] && tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
-}
-
 // ------------------------------------------------------------------ host ----
 
 struct Variant {
@@ -1394,26 +607,13 @@ Variant pick(int n_max) {
     return variant<Cfg<D, 4, 8, 1>>();
 }
 
-cudaError_t launch_tc(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
-    return launch(k_attn_tc, grid, dim3(TcCfg::THREADS), TcCfg::SMEM, s, mk, mv, a);
-}
-
 // Kernel choice for head_dim 128: trees of 33..128 nodes go to the persistent
 // 128-key-tile tcgen05 kernel (k_attn_tq, attn_tq.cu), all others (and
-// head_dim 64) to the mma.sync kernel. TREESPEC_ATTN_KERNEL=mma, tq, tc or kt
-// forces one of them where its limits allow; tc is the earlier 64-key-tile
-// tcgen05 kernel (two softmax streams; with TREESPEC_ATTN_PERSISTENT=1 its
-// persistent form), kt the small-tree tcgen05 kernel (at most 32 nodes, keys on the
-// MMA's M side, key tiles cut evenly over the SMs). Measured on GB300 for a
-// 21-node tree over a 2048-key prefix (batch 8, 32 heads): mma.sync 58 us,
-// kt 81-84 us -- one CTA per SM exposes kt's startup, per-pair epilogues and
-// merges, which the mma.sync kernel's two CTAs per SM overlap.
-bool use_kt(int d, int n_max) {
-    if (d != 128 || n_max > 32) return false;
-    const char *e = getenv("TREESPEC_ATTN_KERNEL");
-    return e && strcmp(e, "kt") == 0;
-}
-
+// head_dim 64) to the mma.sync kernel. TREESPEC_ATTN_KERNEL=mma or tq forces
+// one of them where its limits allow. Measured on GB300: k_attn_tq on a
+// 21-node tree over a 2048-key prefix (batch 8, 32 heads) 52.8 us against
+// 51.2 us for the mma.sync kernel (256 whole-pair items on 152 persistent CTAs
+// leave 104 CTAs with two items and 48 with one).
 bool use_tq(int d, int n_max) {
     if (d != 128 || n_max > 128) return false;
     const char *e = getenv("TREESPEC_ATTN_KERNEL");
@@ -1421,17 +621,7 @@ bool use_tq(int d, int n_max) {
     return n_max > 32;
 }
 
-bool use_tc(int d, int n_max) {
-    if (d != 128 || n_max > TcCfg::NODES) return false;
-    const char *e = getenv("TREESPEC_ATTN_KERNEL");
-    return e && strcmp(e, "tc") == 0;
-}
-
-Variant pick_variant(int d, int n_max) {
-    if (use_tc(d, n_max))
-        return Variant{TcCfg::NODES, TcCfg::THREADS, TcCfg::SMEM, "k_attn_tc", (const void *)k_attn_tc, launch_tc};
-    return d == 64 ? pick<64>(n_max) : pick<128>(n_max);
-}
+Variant pick_variant(int d, int n_max) { return d == 64 ? pick<64>(n_max) : pick<128>(n_max); }
 
 int occupancy(const Variant &v) {
     int occ = 0;
@@ -1454,21 +644,15 @@ int num_sms() {
     return n > 0 ? n : 152;
 }
 
-AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool allow_small_tree) {
-    AttnPlan p{1, 1, 0, 0, false, false, "k_attn_f32"};
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
+    AttnPlan p{1, 1, 0, 0, "k_attn_f32"};
     if (dt != TS_BF16) return p;
-    if (allow_small_tree && use_kt(d, n_max)) {
-        p.n_pad = 32;
-        p.small_tree = true;
-        p.kernel = "k_attn_kt";
-        p.ws_bytes = attn_kt_ws_bytes(B, H);
-        return p;
-    }
     if (use_tq(d, n_max)) {
         p.tq = true;
         p.n_pad = 128;
         p.kernel = "k_attn_tq";
-        p.ws_bytes = 256;
+        p.ws_bytes = kTqQueueBytes;   // the item queue's two counters
+        p.zero_bytes = kTqQueueBytes;
         return p;
     }
     const Variant v = pick_variant(d, n_max);
@@ -1495,14 +679,7 @@ AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool 
     p.n_pad = v.nodes;
     const size_t counters = ((size_t)pairs * 4 + 255) / 256 * 256;
     p.ws_bytes = p.splits > 1 ? counters + (size_t)pairs * p.splits * p.n_pad * (2 + d) * 4 : counters;
-    // The persistent tcgen05 kernel (CTAs walk the (request, head) items)
-    // measured faster only with many short items; TREESPEC_ATTN_PERSISTENT=0/1
-    // overrides.
-    const char *pe = getenv("TREESPEC_ATTN_PERSISTENT");
-    const bool many_items = pairs >= 8LL * num_sms();
-    const bool persistent = pe && *pe ? atoi(pe) != 0 : many_items;
-    p.persistent = p.splits == 1 && use_tc(d, n_max) && persistent;
-    if (p.persistent) p.kernel = "k_attn_tp";
+    p.zero_bytes = counters;
     return p;
 }
 
@@ -1510,9 +687,9 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max, float scale,
                              const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s, const char **why,
                              const PagedArgs &pg) {
-    if (plan.small_tree)
-        return launch_attn_kt(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, ws, status, s, why);
-    if (plan.tq) return launch_attn_tq(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, status, s, why, pg);
+    if (plan.tq)
+        return launch_attn_tq(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, (unsigned *)ws, status, s, why,
+                              pg);
     const Variant v = pick_variant(d, t.n_max);
     CUtensorMap mk, mv;
     // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
@@ -1546,13 +723,6 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
     // longest-first dispatch of the requests (TREESPEC_ATTN_LPT=0: request order)
     const char *lp = getenv("TREESPEC_ATTN_LPT");
     a.lpt = !(lp && *lp && atoi(lp) == 0);
-    if (plan.persistent) {
-        e = cudaFuncSetAttribute(k_attn_tp, cudaFuncAttributeMaxDynamicSharedMemorySize, TpCfg::SMEM);
-        if (e != cudaSuccess) return e;
-        const int pairs = t.B * H;
-        const int grid_p = pairs < num_sms() ? pairs : num_sms();
-        return launch(k_attn_tp, dim3(grid_p), dim3(TpCfg::THREADS), TpCfg::SMEM, s, mk, mv, a);
-    }
     // split index slowest: every first (longest) chunk is dispatched before any later one
     dim3 grid(H, t.B, plan.splits);
     return v.launch(grid, mk, mv, a, s);

@@ -11,9 +11,10 @@
 // The array lives in device memory of every GPU on which the library's device
 // code is loaded, for the life of the process, and holds
 // TS_NOALLOC_SCRATCH_BYTES. Every call on a device shares it: its contents are
-// whatever the previous call left, so the split counters are cleared on the
-// call's stream before each launch, and calls whose kernels overlap on the GPU
-// (different streams, no ordering between them) race on it.
+// whatever the previous call left, so the counters the chosen kernel needs at
+// zero (split counters, or the persistent kernel's item queue) are cleared on
+// the call's stream before each launch, and calls whose kernels overlap on the
+// GPU (different streams, no ordering between them) race on it.
 #include <mutex>
 
 #include "ts_internal.cuh"
@@ -51,30 +52,32 @@ cudaError_t scratch_ptr(void **out) {
 extern "C" ts_status tree_attention_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
                                             const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max,
                                             ts_dtype dtype, float scale, uint32_t *status, cudaStream_t stream) {
-    if (dtype != TS_BF16)   // the fp32 variant uses no workspace: nothing to replace
+    // every check tree_attention makes, before anything is enqueued
+    ts_status st = ts::check_attention_args(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype,
+                                            "tree_attention_noalloc");
+    if (st) return st;
+    if (dtype != TS_BF16)   // the fp32 kernel uses no workspace: nothing to replace
         return tree_attention(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype, scale, nullptr, 0, status,
                               stream);
-    if (!t || t->B < 1 || t->n_max < 1 || t->n_max > TS_MAX_NODES || H < 1 || (d != 64 && d != 128) ||
-        L_max < t->n_max)
-        return tree_attention(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype, scale, nullptr, 0, status,
-                              stream);   // reports the argument error
-    const size_t need = ts::attn_plan(t->B, H, t->n_max, d, L_max, dtype).ws_bytes;
-    if (need > TS_NOALLOC_SCRATCH_BYTES)
+    const ts::AttnPlan plan = ts::attn_plan(t->B, H, t->n_max, d, L_max, dtype);
+    if (plan.ws_bytes > TS_NOALLOC_SCRATCH_BYTES || plan.zero_bytes > plan.ws_bytes)
         return ts::set_error(TS_ERR_INVALID_ARG,
                              "tree_attention_noalloc: these sizes need %zu bytes of scratch, the built-in scratch "
                              "holds %zu (use tree_attention with a caller-provided workspace)",
-                             need, (size_t)TS_NOALLOC_SCRATCH_BYTES);
+                             plan.ws_bytes, (size_t)TS_NOALLOC_SCRATCH_BYTES);
     void *ws = nullptr;
     cudaError_t e = scratch_ptr(&ws);
     if (e != cudaSuccess)
         return ts::set_error(TS_ERR_CUDA, "tree_attention_noalloc: cudaGetSymbolAddress failed: %s",
                              cudaGetErrorString(e));
-    // the split counters must start at zero; clear them on the call's stream
-    const size_t counters = ((size_t)t->B * H * 4 + 255) / 256 * 256;
-    e = cudaMemsetAsync(ws, 0, counters, stream);
-    if (e != cudaSuccess)
-        return ts::set_error(TS_ERR_CUDA, "tree_attention_noalloc: clearing the scratch failed: %s",
-                             cudaGetErrorString(e));
+    // the plan's counters (split counters, or the persistent kernel's item
+    // queue) must start at zero; the previous call may have left anything
+    if (plan.zero_bytes > 0) {
+        e = cudaMemsetAsync(ws, 0, plan.zero_bytes, stream);
+        if (e != cudaSuccess)
+            return ts::set_error(TS_ERR_CUDA, "tree_attention_noalloc: clearing the scratch failed: %s",
+                                 cudaGetErrorString(e));
+    }
     return tree_attention(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype, scale, ws,
                           (size_t)TS_NOALLOC_SCRATCH_BYTES, status, stream);
 }

@@ -6,12 +6,18 @@
 // prefix key and the tree keys of its ancestors and itself (the topology-aware
 // causal mask of sec. 4.2, a bit test on the ancestor bitmask).
 //
-// GB300 design. Each CTA (one per SM) walks (request, head) items p = blockIdx.x,
-// blockIdx.x + gridDim.x, ...; the K/V ring, the two score buffers and the
-// softmax run on across item boundaries.
-//   warp 0    TMA producer (lane 0): 128-key K and V tiles into a 3-stage ring
-//             (64 KB a stage), as 64-key boxes so that a paged cache (pages of
-//             64 keys) is read the same way
+// GB300 design. Each CTA (one per SM) walks (request, head) items: its first
+// item is blockIdx.x, every later one is taken from a queue in the workspace
+// (gridDim.x + an atomic counter), so that CTAs which start late -- their SM
+// still held by a kernel of another stream -- take fewer items instead of
+// finishing last. The K/V ring, the two score buffers and the softmax run on
+// across item boundaries.
+//   warp 0    TMA producer and item queue (lane 0): claims the next item one
+//             item ahead and publishes it in a 4-slot shared-memory ring
+//             (mbarriers iready / ifree) that the other roles read; loads
+//             128-key K and V tiles into a 3-stage ring (64 KB a stage), as
+//             64-key boxes so that a paged cache (pages of 64 keys) is read
+//             the same way
 //   warp 1    MMA issuer (lane 0): S = Q K^T (M = 128 node rows, N = 128 keys,
 //             K = 128 dims) with Q read from TMEM; O += P V (M = 128, N = 128
 //             dims, K = 128 keys) with P read from TMEM
@@ -59,10 +65,14 @@ struct TqCfg {
     static constexpr int OFF_XO = OFF_LS + 4 * NODES * 4; // upper-copy O chunks [2 quarters][2 halves][32][33]
     static constexpr int REQ_CACHE = 512;                 // (n, P) of the first requests, in shared memory
     static constexpr int OFF_REQ = OFF_XO + 4 * 32 * XO_STRIDE * 4;
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1;
+    static constexpr int RING = 4;                        // published items (the queue's shared-memory ring)
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 2 * RING;
     static constexpr int OFF_BAR = OFF_REQ + REQ_CACHE * 8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    // misc ints: [0] TMEM base, [1] timeout, [4..8) item ring, [8..24) the softmax
+    // warps' votes on a ring slot (two sets of eight)
+    static constexpr int MISC_RING = 4, MISC_VOTE = 8;
+    static constexpr int SMEM = OFF_MISC + 128 + 1024;
     static constexpr uint32_t TMEM_COLS = 512, S_COL = 0, O_COL = 256, Q_COL = 384;
 };
 
@@ -87,13 +97,6 @@ __device__ __forceinline__ TqItem tq_item(const AttnArgs &a, const int2 *req, in
     const bool ok = it.n > 0 && it.n <= TqCfg::NODES && it.P >= 0 && it.L <= a.L_max;
     it.ntiles = ok ? (it.L + TqCfg::TKT - 1) / TqCfg::TKT : 0;
     return it;
-}
-
-// The next item after p (stride G) that has key tiles, or -1.
-__device__ __forceinline__ int tq_next(const AttnArgs &a, const int2 *req, int p, int G, int pairs) {
-    for (int q = p + G; q < pairs; q += G)
-        if (tq_item(a, req, q).ntiles > 0) return q;
-    return -1;
 }
 
 // A 32-bit global load issued here (the asm is not moved), its result waited
@@ -130,6 +133,9 @@ __device__ __forceinline__ void pair_sync(int quarter) {
 __device__ __forceinline__ void group_sync(int lq) {
     asm volatile("bar.sync %0, 128;" ::"r"(6 + lq) : "memory");
 }
+
+// Named barrier of the eight softmax warps.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 10, 256;" ::: "memory"); }
 
 // Visibility of the keys k0 .. k0 + 63 of an item for one node row, bit e for
 // key k0 + e: prefix keys visible, tree key t visible iff ancestor bit t (lo:
@@ -194,6 +200,8 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
     const uint32_t sfull = empty + 8 * C::STAGES, pfull = sfull + 16, pvdone = pfull + 16;
     const uint32_t qready = pvdone + 16, ofree = qready + 16, fin = ofree + 8;
+    const uint32_t iready = fin + 8, ifree = iready + 8 * C::RING;
+    volatile int *ring = misc + C::MISC_RING;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((void *)misc)),
@@ -214,6 +222,10 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
         }
         mbar_init(ofree, C::SM_WARPS);
         mbar_init(fin, 1);
+        for (int r = 0; r < C::RING; ++r) {
+            mbar_init(iready + 8 * r, 1);
+            mbar_init(ifree + 8 * r, 1 + C::SM_WARPS);   // the MMA issuer and every softmax warp
+        }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -225,12 +237,37 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     const uint32_t tmem = (uint32_t)misc[0];
 
     if (warp == 0) {
-        if (lane == 0) {   // ---------------------------------------------- TMA producer
-            int g = 0;
-            bool ok = true;
-            for (int p = blockIdx.x; p < pairs && ok; p += G) {
+        if (lane == 0) {   // ---------------------------------------------- TMA producer, item queue
+            // the next item with key tiles (the first: blockIdx.x; later ones
+            // gridDim.x + the queue counter), -1 when none is left
+            auto claim = [&](bool first) -> int {
+                for (int p = first ? (int)blockIdx.x : G + (int)atomicAdd(&a.counters[0], 1u); p < pairs;
+                     p = G + (int)atomicAdd(&a.counters[0], 1u)) {
+                    const TqItem it = tq_item(a, req_s, p);
+                    if (it.ntiles > 0) return p;
+                    if (it.n > 0 && it.h == 0) flag(a.status, TS_STATUS_INDEX);
+                }
+                return -1;
+            };
+            // item k of this CTA into ring slot k % RING, once the item that used
+            // the slot before has been released by every reader
+            auto publish = [&](int k, int p) -> bool {
+                const int r = k % C::RING;
+                if (k >= C::RING && !mbar_wait_bounded(ifree + 8 * r, (uint32_t)(k / C::RING - 1) & 1u)) return false;
+                ring[r] = p;
+                mbar_arrive(iready + 8 * r);
+                return true;
+            };
+            int g = 0, k = 0;
+            int p = claim(true);
+            bool ok = publish(0, p);
+            while (ok && p >= 0) {
+                const int pn = claim(false);   // published before this item's tiles: readers see it an item early
+                if (!publish(k + 1, pn)) {
+                    ok = false;
+                    break;
+                }
                 const TqItem it = tq_item(a, req_s, p);
-                if (it.ntiles == 0 && it.n > 0 && it.h == 0) flag(a.status, TS_STATUS_INDEX);
                 for (int j = 0; j < it.ntiles; ++j, ++g) {
                     const int st = g % C::STAGES, key0 = j * C::TKT;
                     const bool h1 = key0 + C::HALF < it.L;   // the tile's second 64 keys hold any key
@@ -252,6 +289,8 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                         }
                     }
                 }
+                p = pn;
+                ++k;
             }
             if (!ok) misc[1] = 1;
         }
@@ -301,9 +340,13 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             // S(g + 1) is issued before PV(g), also across item boundaries
             int g = 0, u = 0, pend_g = -1, pend_u = 0;
             bool pend_first = false;
-            for (int p = blockIdx.x; p < pairs && ok; p += G) {
+            for (; ok; ++u) {
+                const int r = u % C::RING;
+                if (!mbar_wait_bounded(iready + 8 * r, (uint32_t)(u / C::RING) & 1u)) { ok = false; break; }
+                const int p = ring[r];
+                mbar_arrive(ifree + 8 * r);
+                if (p < 0) break;
                 const TqItem it = tq_item(a, req_s, p);
-                if (it.ntiles == 0) continue;
                 const int qb = u & 1;
                 if (!mbar_wait_bounded(qready + 8 * qb, (uint32_t)(u >> 1) & 1u)) { ok = false; break; }
                 tc_fence_after();
@@ -314,7 +357,6 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                     pend_first = j == 0;
                     pend_u = u;
                 }
-                ++u;
             }
             if (ok && pend_g >= 0) ok = issue_pv(pend_g, pend_first, pend_u);
             if (!ok) misc[1] = 1;
@@ -337,11 +379,29 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
         const int kbz = quarter >= 2 ? hf : 2 + hf;
         float *xo = (float *)(sm + C::OFF_XO) + ((quarter & 1) * 2 + hf) * 32 * C::XO_STRIDE + lane * C::XO_STRIDE;
         bool ok = true;
-        int p = blockIdx.x;
-        while (p < pairs && tq_item(a, req_s, p).ntiles == 0) p += G;
+        // ring slot k (item k of this CTA). Every softmax warp votes with what it
+        // read (INT_MIN: its wait gave up) and all take the common verdict, so
+        // that the warps sharing named barriers always walk the same items.
+        volatile int *vote = misc + C::MISC_VOTE;
+        auto read_slot = [&](int k) -> int {
+            const int r = k % C::RING;
+            int v = INT_MIN;
+            if (ok && mbar_wait_warp(iready + 8 * r, (uint32_t)(k / C::RING) & 1u)) v = ring[r];
+            if (lane == 0) vote[(k & 1) * C::SM_WARPS + (warp - 2)] = v;
+            softmax_sync();   // two vote sets: set k & 1 is rewritten only after every warp passed read k + 1
+            int agreed = vote[(k & 1) * C::SM_WARPS];
+            for (int w = 1; w < C::SM_WARPS; ++w)
+                if (vote[(k & 1) * C::SM_WARPS + w] != agreed) agreed = INT_MIN;
+            if (agreed == INT_MIN) {
+                ok = false;
+                return -1;
+            }
+            return agreed;
+        };
+        int p = read_slot(0);
         int perm_cur = -1;   // perm[b][row] of the current item
         TqAnc anc_cur{0u, 0u, 0u, 0u};   // its ancestor words of this row
-        if (p < pairs) {     // Q of the first item
+        if (p >= 0) {        // Q of the first item
             const TqItem it = tq_item(a, req_s, p);
             perm_cur = row < it.n ? a.t.perm[(size_t)it.b * n_max + row] : -1;
             anc_cur = tq_anc(a, it, row, true);
@@ -351,9 +411,9 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             if (lane == 0) mbar_arrive(qready);
         }
         int g = 0;
-        for (int u = 0; p < pairs; ++u) {
+        for (int u = 0; p >= 0; ++u) {
             const TqItem it = tq_item(a, req_s, p);
-            const int nxt = tq_next(a, req_s, p, G, pairs);
+            const int nxt = read_slot(u + 1);
             const TqItem itn = nxt >= 0 ? tq_item(a, req_s, nxt) : it;
             // the next item's perm entry and ancestor words issued now (used an
             // item later), an L2 prefetch of its Q row a tile later, the Q load
@@ -543,8 +603,11 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(ofree);   // O may be overwritten by the next item now
-            p = nxt < 0 ? pairs : nxt;
+            if (lane == 0) {
+                mbar_arrive(ofree);                   // O may be overwritten by the next item now
+                mbar_arrive(ifree + 8 * (u % C::RING));   // and the item's ring slot reused
+            }
+            p = nxt;
             perm_cur = perm_nxt;
             anc_cur = anc_nxt;
         }
@@ -555,14 +618,23 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     tc_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
-    if (misc[1] && tid == 0) flag(a.status, TS_STATUS_TIMEOUT);
+    if (tid == 0) {
+        if (misc[1]) flag(a.status, TS_STATUS_TIMEOUT);
+        // the last CTA to finish returns the queue to zero for the next launch:
+        // every CTA counted here has stopped claiming items
+        __threadfence();
+        if (atomicAdd(&a.counters[1], 1u) == gridDim.x - 1) {
+            a.counters[0] = 0u;
+            a.counters[1] = 0u;
+        }
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
-                           uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg) {
+                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg) {
     CUtensorMap mk, mv;
     // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
     const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
@@ -585,7 +657,7 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     a.chunk_tiles = 0;
     a.splits = 1;
     a.n_pad = TqCfg::NODES;
-    a.counters = nullptr;
+    a.counters = queue;   // [0] next item - gridDim.x, [1] CTAs finished
     a.part_ml = nullptr;
     a.part_o = nullptr;
     a.status = status;

@@ -98,30 +98,27 @@ cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix
 
 // Split-KV plan shared by the size query and the launch.
 struct AttnPlan {
-    int splits;        // CTAs per (b, h) at most
-    int chunk_tiles;   // 64-key tiles per CTA
-    int n_pad;         // node rows kept per partial
-    size_t ws_bytes;   // partials + counters
-    bool persistent;   // the persistent tcgen05 kernel walks the (b, h) items
-    bool small_tree;   // the small-tree tcgen05 kernel (key tiles cut evenly over the SMs)
+    int splits;          // CTAs per (b, h) at most
+    int chunk_tiles;     // 64-key tiles per CTA
+    int n_pad;           // node rows kept per partial
+    size_t ws_bytes;     // workspace bytes the launch uses
     const char *kernel;  // name of the kernel the launch uses
     bool tq = false;     // the persistent 128-key-tile tcgen05 kernel
+    size_t zero_bytes = 0;   // leading workspace bytes that must be zero before a launch (counters)
 };
-AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt, bool allow_small_tree = true);
+// Workspace of the persistent tcgen05 kernel: its item queue, two unsigned
+// counters (next item, CTAs finished) that the last CTA returns to zero.
+constexpr size_t kTqQueueBytes = 256;
+AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt);
 
 cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, const float *v_cache,
                             const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                             float scale, uint32_t *status, cudaStream_t s);
-// Small-tree tcgen05 kernel (head_dim 128, at most 32 nodes): workspace bytes
-// and launch.
-size_t attn_kt_ws_bytes(int B, int H);
-cudaError_t launch_attn_kt(void *out, const void *q, const void *k_cache, const void *v_cache,
-                           const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale, void *ws,
-                           uint32_t *status, cudaStream_t s, const char **why);
-// Persistent tcgen05 kernel with 128-key tiles (head_dim 128, at most 128 nodes).
+// Persistent tcgen05 kernel with 128-key tiles (head_dim 128, at most 128
+// nodes); queue = the plan's workspace (kTqQueueBytes, zero before the launch).
 cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
-                           uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg);
+                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg);
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,
@@ -131,17 +128,20 @@ size_t greedy_ws_bytes(int B, int n_max, int V);
 cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
                                  int32_t *argmax_out, const float *logits, const ts_tree &t, int V, void *ws,
                                  uint32_t *status, cudaStream_t s);
-cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
                               const float *logits, const int32_t *p_row, int NP, const float *ssm,
                               const int32_t *q_row, int NQ, const float *uniforms, float temperature,
                               const ts_tree &t, int V, uint32_t *status, cudaStream_t s);
 
-cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
                                 const float *logits, const int32_t *p_row, int NP, const float *uniforms,
                                 float temperature, const ts_tree &t, int V, uint32_t *status, cudaStream_t s);
 
 int num_sms();
 
 ts_status set_error(ts_status st, const char *fmt, ...);
+ts_status check_attention_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *prefix_len, const ts_tree *t, int H, int d, int L_max, ts_dtype dtype,
+                               const char *who);
 
 }  // namespace ts

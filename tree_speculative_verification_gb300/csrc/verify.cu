@@ -224,7 +224,12 @@ struct MssShared {
     int bcast_i;
     int pick;
     int token;
+    int lowm;                               // decisions of the walk with a margin below kLowMargin
 };
+// A decision is reported as low-margin when the device's own margin is below
+// this: |u - a| for an accept test, the distance of u * S to the cumulative
+// sums on either side of the drawn token, over S, for a sample.
+constexpr double kLowMargin = 1e-6;
 constexpr size_t kMssHeader = (sizeof(MssShared) + 15) & ~(size_t)15;
 
 // The residual of the current node. With the shared-memory row (R != nullptr)
@@ -315,7 +320,8 @@ __device__ int block_or(MssShared &sm, int x) {
 // drafter rows are read.
 template <bool SMEM_R, bool NAIVE>
 __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
-                                                        const float *logits, const int32_t *p_row, int NP,
+                                                        int32_t *out_lowmargin, const float *logits,
+                                                        const int32_t *p_row, int NP,
                                                         const float *ssm, const int32_t *q_row, int NQ,
                                                         const float *uniforms, float invT, ts_tree t, int V,
                                                         uint32_t *status) {
@@ -330,9 +336,13 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
     int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
     int32_t *op = out_path + (size_t)b * (n_max + 1);
     if (n <= 0) {
-        if (tid == 0) out_count[b] = 0;
+        if (tid == 0) {
+            out_count[b] = 0;
+            if (out_lowmargin) out_lowmargin[b] = 0;
+        }
         return;
     }
+    if (tid == 0) sm.lowm = 0;
     // tree and row indices into shared memory; index checks for every node
     int bad_index = 0;
     for (int i = tid; i < n; i += kMssThreads) {
@@ -357,6 +367,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
     if (block_or(sm, bad_index)) {
         if (tid == 0) {
             out_count[b] = 0;
+            if (out_lowmargin) out_lowmargin[b] = 0;
             flag(status, TS_STATUS_INDEX);
         }
         return;
@@ -461,6 +472,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                     double a = 1.0;
                     if (qx > 0.f) a = fmin(1.0, (double)resid_at(rr, x) / (S * (double)qx));
                     acc = (double)sm.cu[c] <= a;
+                    if (fabs((double)sm.cu[c] - a) < kLowMargin) ++sm.lowm;
                 }
                 sm.pick = bad ? -2 : acc;
             }
@@ -614,6 +626,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         __syncthreads();
         if (warp == 0) {
             int chosen = -1, last_pos = -1;
+            double margin = 0.0;   // stays 0 when rounding left no bracket (the fallback pick)
             if (pick >= 0) {
                 const int ys = pick * per * unit, ye = min(V, ys + per * unit);
                 double carry = sm.base;
@@ -629,8 +642,16 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
                     const double cum = carry + ((double)ch + (double)cl);
                     const unsigned hit = __ballot_sync(0xffffffffu, r > 0.f && cum > target);
                     const unsigned pos = __ballot_sync(0xffffffffu, r > 0.f);
-                    if (hit) chosen = y0 + __ffs(hit) - 1;
-                    else if (pos) last_pos = y0 + 31 - __clz(pos);
+                    if (hit) {
+                        const int hl = __ffs(hit) - 1;
+                        chosen = y0 + hl;
+                        // C(t) and C(t - 1) of the drawn token t, from the lane that holds it
+                        const double c_t = __shfl_sync(0xffffffffu, cum, hl);
+                        const double c_prev = c_t - (double)__shfl_sync(0xffffffffu, r, hl);
+                        margin = total > 0.0 ? fmin(target - c_prev, c_t - target) / total : 0.0;
+                    } else if (pos) {
+                        last_pos = y0 + 31 - __clz(pos);
+                    }
                     carry += (double)__shfl_sync(0xffffffffu, ch, 31) + (double)__shfl_sync(0xffffffffu, cl, 31);
                 }
             }
@@ -638,6 +659,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
             if (lane == 0) {
                 ot[cnt] = chosen;
                 sm.token = chosen;
+                if (margin < kLowMargin) ++sm.lowm;
             }
         }
         ++cnt;
@@ -657,6 +679,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         if (next < 0) break;
         u = next;
     }
+    __syncthreads();
     if (tid == 0) {
         if (nonfinite) {
             out_count[b] = 0;
@@ -664,6 +687,7 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
         } else {
             out_count[b] = cnt;
         }
+        if (out_lowmargin) out_lowmargin[b] = sm.lowm;
     }
 }
 
@@ -699,7 +723,8 @@ cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t
 }
 
 template <bool NAIVE>
-cudaError_t launch_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
+cudaError_t launch_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                        const float *logits,
                         const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
                         const float *uniforms, float temperature, const ts_tree &t, int V, uint32_t *status,
                         cudaStream_t s) {
@@ -712,25 +737,26 @@ cudaError_t launch_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_cou
             cudaFuncSetAttribute(k_mss<true, NAIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)with_row);
         if (e != cudaSuccess) return e;
         return launch(k_mss<true, NAIVE>, dim3(t.B), dim3(kMssThreads), with_row, s, out_tokens, out_path, out_count,
-                      logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+                      out_lowmargin, logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
     }
     return launch(k_mss<false, NAIVE>, dim3(t.B), dim3(kMssThreads), (size_t)kMssHeader, s, out_tokens, out_path,
-                  out_count, logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+                  out_count, out_lowmargin, logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V,
+                  status);
 }
 
-cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
-                              const int32_t *p_row, int NP, const float *ssm, const int32_t *q_row, int NQ,
-                              const float *uniforms, float temperature, const ts_tree &t, int V,
-                              uint32_t *status, cudaStream_t s) {
-    return launch_walk<false>(out_tokens, out_path, out_count, logits, p_row, NP, ssm, q_row, NQ, uniforms,
-                              temperature, t, V, status, s);
+cudaError_t launch_verify_mss(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                              const float *logits, const int32_t *p_row, int NP, const float *ssm,
+                              const int32_t *q_row, int NQ, const float *uniforms, float temperature,
+                              const ts_tree &t, int V, uint32_t *status, cudaStream_t s) {
+    return launch_walk<false>(out_tokens, out_path, out_count, out_lowmargin, logits, p_row, NP, ssm, q_row, NQ,
+                              uniforms, temperature, t, V, status, s);
 }
 
-cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, const float *logits,
-                                const int32_t *p_row, int NP, const float *uniforms, float temperature,
-                                const ts_tree &t, int V, uint32_t *status, cudaStream_t s) {
-    return launch_walk<true>(out_tokens, out_path, out_count, logits, p_row, NP, nullptr, nullptr, 1, uniforms,
-                             temperature, t, V, status, s);
+cudaError_t launch_verify_naive(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *out_lowmargin,
+                                const float *logits, const int32_t *p_row, int NP, const float *uniforms,
+                                float temperature, const ts_tree &t, int V, uint32_t *status, cudaStream_t s) {
+    return launch_walk<true>(out_tokens, out_path, out_count, out_lowmargin, logits, p_row, NP, nullptr, nullptr, 1,
+                             uniforms, temperature, t, V, status, s);
 }
 
 }  // namespace ts

@@ -53,6 +53,7 @@ class DeviceStep:
         self.mss_tokens = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
         self.mss_path = torch.full((B, n_max + 1), -1, dtype=torch.int32, device=dev)
         self.mss_count = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.mss_lowmargin = torch.zeros(B, dtype=torch.int32, device=dev)
         self.argmax = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
         self.ws_greedy = api.workspace(api.TS_OP_VERIFY_GREEDY, B, n_max=n_max, V=w.V, device=dev)
         self._side = None   # verification stream, created on first use
@@ -97,10 +98,11 @@ class DeviceStep:
         if kind in ("mss", "both"):
             api.verify_mss(self.mss_tokens, self.mss_path, self.mss_count, self.logits, self.ssm, self.q_row,
                            self.uniforms, self.w.temperature, self.tree, p_row=self.p_row, status=self.status,
-                           stream=stream)
+                           stream=stream, lowmargin=self.mss_lowmargin)
         if kind == "naive":
             api.verify_naive(self.mss_tokens, self.mss_path, self.mss_count, self.logits, self.uniforms,
-                             self.w.temperature, self.tree, p_row=self.p_row, status=self.status, stream=stream)
+                             self.w.temperature, self.tree, p_row=self.p_row, status=self.status, stream=stream,
+                             lowmargin=self.mss_lowmargin)
 
     def commit(self, kind: str | None = None, stream=None):
         kind = kind or self.w.verify

@@ -24,6 +24,8 @@ Array conventions (every per-node array is in *input node order*):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -109,24 +111,43 @@ def _pad(a: np.ndarray, n_max: int, fill) -> np.ndarray:
 
 
 def _qkv(rng, B, n_max, H, d, L_max, prefix_len, dtype, scale=1.0):
-    """Q, K_new, V_new for the tree nodes and the K/V prefix cache, N(0, scale^2)."""
-    def draw(shape):
-        x = rng.standard_normal(shape, dtype=np.float32)
+    """Q, K_new, V_new for the tree nodes and the K/V prefix cache, N(0, scale^2).
+    The prefix K/V of request b comes from its own child generator
+    (rng.spawn(B)[b]: K, then V), so the requests are drawn on several threads
+    with a result that does not depend on the thread count."""
+    def draw(g, shape):
+        x = g.standard_normal(shape, dtype=np.float32)
         if scale != 1.0:
             x *= np.float32(scale)
         return f32_to_bf16_bits(x) if dtype == "bf16" else x
 
-    q = draw((B, n_max, H, d))
-    k_new = draw((B, n_max, H, d))
-    v_new = draw((B, n_max, H, d))
+    q = draw(rng, (B, n_max, H, d))
+    k_new = draw(rng, (B, n_max, H, d))
+    v_new = draw(rng, (B, n_max, H, d))
     cdt = np.uint16 if dtype == "bf16" else np.float32
     k_cache = np.zeros((B, H, L_max, d), cdt)
     v_cache = np.zeros((B, H, L_max, d), cdt)
-    for b in range(B):
+    children = rng.spawn(B)
+
+    def fill(b):
         P = int(prefix_len[b])
-        k_cache[b, :, :P] = draw((H, P, d))
-        v_cache[b, :, :P] = draw((H, P, d))
+        k_cache[b, :, :P] = draw(children[b], (H, P, d))
+        v_cache[b, :, :P] = draw(children[b], (H, P, d))
+
+    with ThreadPoolExecutor(max_workers=min(B, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(B)))
     return q, k_new, v_new, k_cache, v_cache
+
+
+def _topk_stable(row: np.ndarray, k: int) -> np.ndarray:
+    """The k largest entries of row, best first, ties to the lower index: the
+    first k of a stable argsort of -row, without sorting the whole row."""
+    if k >= row.size:
+        return np.argsort(-row, kind="stable")[:k]
+    thr = np.partition(row, row.size - k)[row.size - k]     # the k-th largest value
+    cand = np.nonzero(row >= thr)[0]                         # increasing index
+    order = np.lexsort((cand, -row[cand]))                   # by value desc, then index asc
+    return cand[order][:k]
 
 
 def _round_up(x, m):
@@ -180,7 +201,7 @@ def _expansion_workload(rng, *, name, B, H, d, dtype, P, widths, V, sigma_t, sig
             k = len(kids)
             if plant == "topk":
                 # the drafter's top-k tokens at u, best first
-                order = np.argsort(-ssm[b, u], kind="stable")[:k]
+                order = _topk_stable(ssm[b, u], k)
                 tokens[b, kids] = order
             else:
                 # first child = target argmax with probability `plant`, the other
