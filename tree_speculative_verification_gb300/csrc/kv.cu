@@ -65,74 +65,92 @@ __global__ void __launch_bounds__(kKvThreads) k_kv_append(uint4 *k_cache, uint4 
     }
 }
 
-// One CTA per (head, request). Path node i moves from row P + dfs(path[i]) to
-// row P + i. In each round every thread first reads its 16-byte pieces and,
-// after a barrier, writes them; a round's destinations (rows P + i) can never
-// be a later round's sources, because a node's DFS index is at least its
-// depth, dfs(path[i']) >= i'.
-__global__ void __launch_bounds__(kKvThreads) k_kv_commit(uint4 *k_cache, uint4 *v_cache, const int32_t *prefix_len,
-                                                          int32_t *new_prefix_len, const int32_t *out_path,
-                                                          const int32_t *out_count, ts_tree t, int H, int row_vec,
-                                                          int L_max, uint32_t *status, PagedArgs pg) {
-    const int b = blockIdx.y, h = blockIdx.x, tid = threadIdx.x;
+// One CTA per request, every head. Path node i moves from row P + dfs(path[i])
+// to row P + i. The counts, the path and the request's whole depth-first map
+// are fetched in one round trip; then the moves go in rounds of increasing
+// path index, each round reading all its 16-byte pieces and, after a barrier,
+// writing them. A round's destinations (rows P + i) are never a later round's
+// sources, because a node's DFS index is at least its depth,
+// dfs(path[i']) >= i' > i; rows already in place (dfs(path[i]) == i) are not
+// copied.
+constexpr int kCommitThreads = 512, kCommitPer = 4;
+
+__global__ void __launch_bounds__(kCommitThreads) k_kv_commit(uint4 *k_cache, uint4 *v_cache, const int32_t *prefix_len,
+                                                              int32_t *new_prefix_len, const int32_t *out_path,
+                                                              const int32_t *out_count, ts_tree t, int H, int row_vec,
+                                                              int L_max, uint32_t *status, PagedArgs pg) {
+    const int b = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
-    const int n = t.n_nodes[b], P = prefix_len[b];
-    const int cnt = out_count[b];
-    __shared__ int src_s[kMaxNodes + 1];
+    __shared__ int dfs_s[kMaxNodes], src_s[kMaxNodes + 1];
+    __shared__ long long from_s[kMaxNodes + 1], to_s[kMaxNodes + 1];   // cache rows of head 0
     __shared__ int bad_s;
-    // the path entries are read alongside the counts (no dependent round trip)
+    const int n = t.n_nodes[b], P = prefix_len[b], cnt = out_count[b];
     const int32_t *path = out_path + (size_t)b * (t.n_max + 1);
     const int v_mine = tid <= t.n_max ? path[tid] : -1;
+    const int dfs_mine = tid < t.n_max ? t.dfs_of[(size_t)b * t.n_max + tid] : -1;
     if (tid == 0) bad_s = !(n > 0 && cnt >= 0 && cnt <= n && P >= 0 && P + n <= L_max);
+    if (tid < t.n_max) dfs_s[tid] = dfs_mine;
     __syncthreads();
     if (!bad_s && tid < cnt) {
         if (v_mine < 0 || v_mine >= n) bad_s = 1;
-        else src_s[tid] = t.dfs_of[(size_t)b * t.n_max + v_mine];
+        else src_s[tid] = dfs_s[v_mine];
     }
     __syncthreads();
     if (bad_s) {
-        if (h == 0 && tid == 0) {
+        if (tid == 0) {
             if (cnt != 0 || (n > 0 && (P < 0 || P + n > L_max))) flag(status, TS_STATUS_INDEX);
             new_prefix_len[b] = P;
         }
         return;
     }
-    // cache rows of the moves: source P + dfs(path[i]), destination P + i
-    __shared__ long long from_s[kMaxNodes + 1], to_s[kMaxNodes + 1];
+    // rows of head h are those of head 0 plus h * hs (dense strips of L_max
+    // rows, or pages holding TS_PAGE_KEYS rows of every head)
+    const long long hs = pg.bt ? TS_PAGE_KEYS : L_max;
     if (tid < cnt) {
-        from_s[tid] = cache_row(pg, b, h, H, L_max, P + src_s[tid]);
-        to_s[tid] = cache_row(pg, b, h, H, L_max, P + tid);
+        from_s[tid] = cache_row(pg, b, 0, H, L_max, P + src_s[tid]);
+        to_s[tid] = cache_row(pg, b, 0, H, L_max, P + tid);
         if (from_s[tid] < 0 || to_s[tid] < 0) bad_s = 1;
     }
     __syncthreads();
     if (bad_s) {
-        if (h == 0 && tid == 0) {
+        if (tid == 0) {
             flag(status, TS_STATUS_INDEX);
             new_prefix_len[b] = P;
         }
         return;
     }
-    const int total = cnt * row_vec;
-    for (int r0 = 0; r0 < total; r0 += kKvThreads) {
-        const int idx = r0 + tid;
-        uint4 kx, vx;
-        int i = 0, c = 0;
-        const bool mine = idx < total;
-        if (mine) {
-            i = idx / row_vec;
-            c = idx - i * row_vec;
-            kx = k_cache[(size_t)from_s[i] * row_vec + c];
-            vx = v_cache[(size_t)from_s[i] * row_vec + c];
+    const int per_i = H * row_vec;   // pieces of one path node, all heads
+    const int total = cnt * per_i;
+    for (int r0 = 0; r0 < total; r0 += kCommitThreads * kCommitPer) {
+        uint4 kx[kCommitPer], vx[kCommitPer];
+        size_t dst[kCommitPer];
+        bool mv[kCommitPer];
+#pragma unroll
+        for (int k = 0; k < kCommitPer; ++k) {
+            const int idx = r0 + k * kCommitThreads + tid;
+            mv[k] = false;
+            if (idx < total) {
+                const int i = idx / per_i, rem = idx - i * per_i, h = rem / row_vec, c = rem - h * row_vec;
+                if (src_s[i] != i) {
+                    mv[k] = true;
+                    const size_t src = (size_t)(from_s[i] + h * hs) * row_vec + c;
+                    dst[k] = (size_t)(to_s[i] + h * hs) * row_vec + c;
+                    kx[k] = k_cache[src];
+                    vx[k] = v_cache[src];
+                }
+            }
         }
         __syncthreads();
-        if (mine && src_s[i] != i) {
-            k_cache[(size_t)to_s[i] * row_vec + c] = kx;
-            v_cache[(size_t)to_s[i] * row_vec + c] = vx;
-        }
+#pragma unroll
+        for (int k = 0; k < kCommitPer; ++k)
+            if (mv[k]) {
+                k_cache[dst[k]] = kx[k];
+                v_cache[dst[k]] = vx[k];
+            }
         __syncthreads();
     }
-    if (h == 0 && tid == 0) new_prefix_len[b] = P + cnt;
+    if (tid == 0) new_prefix_len[b] = P + cnt;
 }
 
 }  // namespace
@@ -150,8 +168,7 @@ cudaError_t launch_kv_commit(void *k_cache, void *v_cache, const int32_t *prefix
                              const int32_t *out_path, const int32_t *out_count, const ts_tree &t, int H, int d,
                              int L_max, int esize, uint32_t *status, cudaStream_t s, const PagedArgs &pg) {
     const int row_vec = d * esize / 16;
-    dim3 grid(H, t.B);
-    return launch(k_kv_commit, grid, dim3(kKvThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, prefix_len,
+    return launch(k_kv_commit, dim3(t.B), dim3(kCommitThreads), 0, s, (uint4 *)k_cache, (uint4 *)v_cache, prefix_len,
                   new_prefix_len, out_path, out_count, t, H, row_vec, L_max, status, pg);
 }
 
