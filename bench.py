@@ -304,7 +304,7 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def _load_step(name, args, device, verify=None):
+def _load_step(name, args, device, verify=None, paged=False, serial_verify=False):
     from tree_speculative_verification_gb300 import api, workloads
     from tree_speculative_verification_gb300.step import DeviceStep
     w = workloads.make(name, scale_down=args.scale_down)
@@ -312,7 +312,7 @@ def _load_step(name, args, device, verify=None):
         if verify in ("mss", "both") and w.ssm is None:
             raise SystemExit(f"--verify {verify}: the {name} workload has no drafter distributions")
         w.verify = verify
-    s = DeviceStep(w, device)
+    s = DeviceStep(w, device, paged=paged, serial_verify=serial_verify)
     s.run(w.verify)
     import torch
     torch.cuda.synchronize()
@@ -428,7 +428,7 @@ def run_ours(args):
     from tree_speculative_verification_gb300 import api, workloads
     api.load_library()
     stream = torch.cuda.current_stream(device)
-    w, s = _load_step(args.config, args, device, args.verify)
+    w, s = _load_step(args.config, args, device, args.verify, paged=args.paged, serial_verify=args.serial_verify)
     kind = w.verify
     nodes_per_step = int(w.n_nodes_dev.sum())
     accepted_per_step = s.accepted(kind)
@@ -470,6 +470,7 @@ def run_ours(args):
     seq_line = None
     if args.sequence_baseline and rank == 0:
         seq_line = measure_sequence_baseline(w, K, device, stream, t_att)
+    sweep = measure_sequence_sweep(K, device, stream) if args.sequence_sweep and rank == 0 else None
     ms_per_step, value = replica_rate(ms / args.steps, nodes_per_step, dist, device)
 
     # ---- end to end through the C ABI with host buffers: pinned inputs in, results out
@@ -518,10 +519,68 @@ def run_ours(args):
             **({"sequence_baseline": seq_line} if seq_line else {}),
             "accepted_tokens_per_s": ws * accepted_per_step / (ms_per_step * 1e-3),
             "gpu_launches": launches,
-            **({"per_config": per_config} if per_config else {})}
+            **({"per_config": per_config} if per_config else {}),
+            **({"sequence_sweep": sweep} if sweep else {}),
+            **({"cache": "paged (pages of 64 keys, randomly placed)"} if args.paged else {}),
+            **({"step_order": "verification after attention on one stream"} if args.serial_verify else {})}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _graph_time(fn, K, device, stream):
+    """Milliseconds per call of fn from a CUDA graph of K back-to-back calls."""
+    import torch
+    ge = _events(2, True)
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(device)
+    cs.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+        cur = torch.cuda.current_stream(device)
+        ge[0].record(cur)
+        for _ in range(K):
+            fn()
+        ge[1].record(cur)
+    stream.wait_stream(cs)
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    return ge[0].elapsed_time(ge[1]) / K
+
+
+def measure_sequence_sweep(K, device, stream, batches=(1, 2, 4, 8, 16)):
+    """SpecInfer Fig. 11 on this GPU, for the attention layer: the LLaMA-7B-shaped
+    layer (32 heads x 128, prefix 2048, expansion tree (1,1,3,1,1,1,1,1), 21
+    nodes and 3 root-to-leaf paths per request) at several batch sizes, tree
+    attention against sequence-based attention (one sequence and one prefix
+    copy per path), each timed as a graph of K back-to-back launches."""
+    import torch
+    from tree_speculative_verification_gb300 import api, workloads
+    from tree_speculative_verification_gb300.step import DeviceStep
+    rows = []
+    for B in batches:
+        w = workloads.make("llama7b", batch=B)
+        tree = DeviceStep(w, device)
+        tree.build()
+        tree.append()
+        seq_w, _ = workloads.sequence_batch(w)
+        seq_w.n_nodes_dev = seq_w.n_nodes
+        seq = DeviceStep(seq_w, device)
+        seq.build()
+        seq.append()
+        torch.cuda.synchronize()
+        t_tree = _graph_time(tree.attend, K, device, stream)
+        t_seq = _graph_time(seq.attend, K, device, stream)
+        w.n_nodes_dev = w.n_nodes
+        bf = api.TS_BF16
+        rows.append({"batch": B, "tree_ms": t_tree, "sequence_ms": t_seq, "ratio": t_seq / t_tree,
+                     "paths": int(seq_w.B), "tree_bytes": attention_bytes(w), "sequence_bytes": attention_bytes(seq_w),
+                     "tree_kernel": api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, bf),
+                     "sequence_kernel": api.attention_kernel(seq_w.B, seq_w.H, seq_w.n_max, seq_w.d, seq_w.L_max, bf)})
+        del tree, seq
+        torch.cuda.empty_cache()
+    return rows
 
 
 def measure_sequence_baseline(w, K, device, stream, t_att):
@@ -665,6 +724,11 @@ def main():
                     help="also time attention as one sequence per root-to-leaf path (SpecInfer Fig. 4 left)")
     ap.add_argument("--verify", default=None, choices=["greedy", "mss", "naive", "both"],
                     help="verifier of the step (default: the workload's)")
+    ap.add_argument("--sequence-sweep", action="store_true",
+                    help="tree vs sequence-based attention on the LLaMA-7B-shaped layer at batch 1, 2, 4, 8, 16")
+    ap.add_argument("--paged", action="store_true", help="the KV cache in pages of 64 keys (paged calls)")
+    ap.add_argument("--serial-verify", action="store_true",
+                    help="verification after the attention on one stream (no overlap)")
     ap.add_argument("--eager", action="store_true", help="launch every step from the host instead of a CUDA graph")
     ap.add_argument("--scale-down", type=int, default=1,
                     help="divide the batch (and the long prefix) by N: a smaller case of the same kernels, for profiling")

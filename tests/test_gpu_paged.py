@@ -173,3 +173,28 @@ def test_paged_bad_page_id_sets_index():
                              st)
     torch.cuda.synchronize()
     assert st.item() & api.STATUS_INDEX
+
+
+def test_paged_step_equals_dense_step():
+    """The merge workload's whole step (chain merge, append, attention, MSS,
+    commit) on a paged cache: attention output, accepted tokens and the
+    committed rows equal the dense step's bit for bit."""
+    from tree_speculative_verification_gb300.step import DeviceStep
+    from _helpers import workload
+    w = workload("merge")
+    dense, paged = DeviceStep(w), DeviceStep(w, paged=True, seed=7)
+    dense.run("mss")
+    paged.run("mss")
+    torch.cuda.synchronize()
+    assert dense.status.item() & ~api.STATUS_ZERO_RESID == 0 and paged.status.item() == dense.status.item()
+    assert np.array_equal(_bits(paged.out), _bits(dense.out))
+    assert torch.equal(paged.mss_tokens, dense.mss_tokens) and torch.equal(paged.mss_count, dense.mss_count)
+    assert torch.equal(paged.new_prefix_len, dense.new_prefix_len)
+    bt = paged.kv.block_table.cpu().numpy()
+    got_k = _dense_from_pages(_bits(paged.kv.k_pages), bt, w.B, w.H, w.L_max, w.d)
+    got_v = _dense_from_pages(_bits(paged.kv.v_pages), bt, w.B, w.H, w.L_max, w.d)
+    npl = dense.new_prefix_len.cpu().numpy()
+    ref_k, ref_v = _bits(dense.k_cache), _bits(dense.v_cache)
+    for b in range(w.B):     # every row up to the new prefix length
+        assert np.array_equal(got_k[b, :, :npl[b]], ref_k[b, :, :npl[b]]), b
+        assert np.array_equal(got_v[b, :, :npl[b]], ref_v[b, :, :npl[b]]), b

@@ -576,6 +576,11 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = 0.f;
                 }
+                if (q2 == 1) {   // O is read out: the next item's first PV may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ofree);
+                }
                 if constexpr (DUP) {   // the upper copy's partial row goes to its lower twin
                     if (upper) {
 #pragma unroll
@@ -601,12 +606,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(ofree);                   // O may be overwritten by the next item now
-                mbar_arrive(ifree + 8 * (u % C::RING));   // and the item's ring slot reused
-            }
+            if (lane == 0) mbar_arrive(ifree + 8 * (u % C::RING));   // the item's ring slot may be reused
             p = nxt;
             perm_cur = perm_nxt;
             anc_cur = anc_nxt;

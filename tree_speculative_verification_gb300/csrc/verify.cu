@@ -15,6 +15,7 @@
 #include <float.h>
 #include <math.h>
 
+#include "attn_common.cuh"
 #include "ts_internal.cuh"
 
 namespace ts {
@@ -691,6 +692,427 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
     }
 }
 
+// -------------------------------------------------- MSS / naive walk, fast form ----
+// The same walk (Algorithm 2, VerifyStochastic; or naive sampling) for rows
+// that fit shared memory with V a multiple of 4 and 16-byte aligned rows:
+//  * warp w owns the contiguous float4 range [w C4, (w + 1) C4) of the
+//    vocabulary in every pass (lane-consecutive 16-byte shared-memory accesses,
+//    no bank conflicts), so the per-warp partial sums of a pass are also the
+//    coarse level of the inverse CDF;
+//  * the visited node's target row arrives by bulk copy (TMA engine) into the
+//    residual buffer R, completing on an mbarrier;
+//  * block reductions are float-float: every warp writes its partial, one
+//    barrier, and every warp combines the 32 partials itself (identical
+//    results: the butterfly and the float-float add are symmetric), into
+//    double-buffered slots, so each reduction costs one barrier;
+//  * a child's test needs no barrier: the pass before it records R at the
+//    child's token (double-buffered), and every warp takes the same verdict.
+// Elementwise arithmetic is the same fp32 as k_mss; sums are compensated fp32
+// per thread, float-float across threads; ratio and CDF tests in fp32 /
+// float-float (no fp64 in per-thread code: GB300's fp64 rate is low).
+constexpr int kWalkThreads = 1024;
+constexpr int kWalkWarps = kWalkThreads / 32;
+constexpr uint32_t kBulkChunk = 32768;
+
+struct WalkShared {
+    float red_mx[2][kWalkWarps];
+    float red_hi[2][kWalkWarps], red_lo[2][kWalkWarps];
+    int red_bad[2][kWalkWarps];
+    float cq[kMaxNodes];                    // q_c(x_c) of each child of the current node
+    float cu[kMaxNodes];                    // its accept uniform
+    int depth[kMaxNodes];
+    int perm[kMaxNodes];
+    int tok[kMaxNodes];
+    int sub_end[kMaxNodes];
+    int prow[kMaxNodes];
+    int qrow[kMaxNodes];
+    const float *rej_q[kMaxNodes];
+    float rej_S[kMaxNodes];
+    float rx[2];                            // R at the token of the next child to test
+    float us;                               // the final-sample uniform of the current node
+    int chosen;
+    int lowm;
+    unsigned long long bar;                 // completion of the row's bulk copy
+};
+constexpr size_t kWalkHeader = (sizeof(WalkShared) + 127) & ~(size_t)127;
+
+__device__ __forceinline__ float pick4(const float4 &a, int e) {
+    return e == 0 ? a.x : (e == 1 ? a.y : (e == 2 ? a.z : a.w));
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ void warp_ff_sum(float &h, float &l) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float bh = __shfl_xor_sync(0xffffffffu, h, o), bl = __shfl_xor_sync(0xffffffffu, l, o);
+        ff_add(h, l, bh, bl);
+    }
+}
+
+// a > b for normalised float-float values
+__device__ __forceinline__ bool ff_gt(float ah, float al, float bh, float bl) {
+    return ah > bh || (ah == bh && al > bl);
+}
+
+// (h, l) * x as float-float (exact product of the high part, plus the low part's)
+__device__ __forceinline__ void ff_mul_f(float h, float l, float x, float &oh, float &ol) {
+    const float p = h * x;
+    const float e = __fmaf_rn(h, x, -p) + l * x;
+    oh = p + e;
+    ol = e - (oh - p);
+}
+
+// Block maximum (and OR of a flag), the same in every warp; one barrier.
+__device__ float walk_max(WalkShared &sm, int k, float x, int flag_in, int &flag_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    x = warp_max(x);
+    flag_in = __any_sync(0xffffffffu, flag_in);
+    if (lane == 0) {
+        sm.red_mx[k & 1][warp] = x;
+        sm.red_bad[k & 1][warp] = flag_in;
+    }
+    __syncthreads();
+    flag_out = __any_sync(0xffffffffu, sm.red_bad[k & 1][lane]);
+    return warp_max(sm.red_mx[k & 1][lane]);
+}
+
+// Block float-float sum, the same in every warp; the warps' partials stay in
+// slot k & 1 (the coarse level of the inverse CDF). One barrier.
+__device__ void walk_sum(WalkShared &sm, int k, float &h, float &l) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    warp_ff_sum(h, l);
+    if (lane == 0) {
+        sm.red_hi[k & 1][warp] = h;
+        sm.red_lo[k & 1][warp] = l;
+    }
+    __syncthreads();
+    h = sm.red_hi[k & 1][lane];
+    l = sm.red_lo[k & 1][lane];
+    warp_ff_sum(h, l);
+}
+
+template <bool NAIVE>
+__global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_count,
+                                                          int32_t *out_lowmargin, const float *logits,
+                                                          const int32_t *p_row, int NP, const float *ssm,
+                                                          const int32_t *q_row, int NQ, const float *uniforms,
+                                                          float invT, ts_tree t, int V, uint32_t *status) {
+    extern __shared__ __align__(128) unsigned char walk_smem[];
+    WalkShared &sm = *reinterpret_cast<WalkShared *>(walk_smem);
+    float *R = reinterpret_cast<float *>(walk_smem + kWalkHeader);
+    float4 *R4 = reinterpret_cast<float4 *>(R);
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bar = smem_u32(&sm.bar);
+    pdl_wait();
+    pdl_trigger();
+    const int n = t.n_nodes[b];
+    const int n_max = t.n_max;
+    int32_t *ot = out_tokens + (size_t)b * (n_max + 1);
+    int32_t *op = out_path + (size_t)b * (n_max + 1);
+    if (n <= 0) {
+        if (tid == 0) {
+            out_count[b] = 0;
+            if (out_lowmargin) out_lowmargin[b] = 0;
+        }
+        return;
+    }
+    if (tid == 0) {
+        sm.lowm = 0;
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // tree and row indices into shared memory; index checks for every node
+    int bad_index = 0;
+    for (int i = tid; i < n; i += kWalkThreads) {
+        const size_t o = (size_t)b * n_max + i;
+        const int v = t.perm[o];
+        sm.perm[i] = v;
+        sm.tok[i] = t.token[o];
+        sm.sub_end[i] = t.sub_end[o];
+        sm.depth[i] = t.depth[o];
+        const int pr = p_row ? p_row[(size_t)b * n_max + v] : v;
+        sm.prow[i] = pr;
+        if (pr < 0 || pr >= NP) bad_index = 1;
+        if (i > 0 && NAIVE) {
+            if (sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
+        } else if (i > 0) {
+            const int qr = q_row[(size_t)b * n_max + v];
+            sm.qrow[i] = qr;
+            if (qr < 0 || qr >= NQ || sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
+        }
+    }
+    // per-warp flags through a reduction slot that the walk's first use of it
+    // (an odd-numbered maximum) overwrites only behind later barriers
+    bad_index = __any_sync(0xffffffffu, bad_index);
+    if (lane == 0) sm.red_bad[1][warp] = bad_index;
+    __syncthreads();
+    if (__any_sync(0xffffffffu, sm.red_bad[1][lane])) {
+        if (tid == 0) {
+            out_count[b] = 0;
+            if (out_lowmargin) out_lowmargin[b] = 0;
+            flag(status, TS_STATUS_INDEX);
+        }
+        return;
+    }
+    const float *u_acc = uniforms + (size_t)b * 2 * n_max;
+    const float *u_smp = u_acc + n_max;
+    const int V4 = V >> 2;
+    const int C4 = (V4 + kWalkWarps - 1) / kWalkWarps;          // float4s of a warp's chunk
+    const int g0 = min(V4, warp * C4), g1 = min(V4, g0 + C4);     // this warp's chunk
+    int u = 0, cnt = 0, nonfinite = 0, timeout = 0;
+    int k = 0;            // reductions so far (slot parity)
+    uint32_t visit = 0;   // bulk copies so far (mbarrier phase)
+    if (tid == 0) op[0] = sm.perm[0];
+
+    for (int step = 0; step < n; ++step) {
+        const float *row = logits + ((size_t)b * NP + sm.prow[u]) * V;
+        const int du = sm.depth[u], se_u = sm.sub_end[u];
+        // the node's row into R by bulk copy (every earlier access of R is
+        // behind the last barrier; the proxy fence orders them before the copy)
+        if (tid == 0) {
+            fence_async_smem();
+            mbar_expect_tx(bar, (uint32_t)V * 4u);
+            for (uint32_t off = 0; off < (uint32_t)V * 4u; off += kBulkChunk)
+                bulk_g2s(smem_u32(R) + off, (const char *)row + off, min(kBulkChunk, (uint32_t)V * 4u - off), bar);
+        }
+        // meanwhile: the values the tests read (q_c(x_c), accept uniforms), the
+        // final-sample uniform. (Pulling the children's drafter rows into L2 here
+        // measured slower: merge workload 62.9 vs 59.6 us per call.)
+        for (int i = u + 1 + tid; !NAIVE && i < se_u; i += kWalkThreads)
+            if (sm.depth[i] == du + 1) {
+                sm.cq[i] = __ldg(ssm + ((size_t)b * NQ + sm.qrow[i]) * V + sm.tok[i]);
+                sm.cu[i] = __ldg(u_acc + sm.perm[i]);
+            }
+        if (tid == kWalkThreads - 1) sm.us = __ldg(u_smp + sm.perm[u]);
+        const bool landed = mbar_wait_bounded(bar, visit & 1u);
+        ++visit;
+        // pass 1: maximum of the row (of the tempered logits: invT > 0), finiteness
+        float mx = -FLT_MAX;
+        int nf = 0;
+        if (landed)
+            for (int g = g0 + lane; g < g1; g += 32) {
+                const float4 a = R4[g];
+                nf |= !isfinite(a.x) | !isfinite(a.y) | !isfinite(a.z) | !isfinite(a.w);
+                mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+            }
+        int tmo = 0;
+        const float mxb = walk_max(sm, k++, nf ? INFINITY : mx, !landed, tmo);
+        if (tmo) { timeout = 1; break; }
+        if (mxb == INFINITY) { nonfinite = 1; break; }
+        const float m = mxb * invT;
+        // pass 2: e = 2^((l/T - m) log2 e), R = e, S = sum e; R at the first child's token
+        const int c_first = u + 1 < se_u ? u + 1 : -1;
+        const int x_first = (!NAIVE && c_first >= 0) ? sm.tok[c_first] : -1;
+        float s = 0.f, cc = 0.f;
+        for (int g = g0 + lane; g < g1; g += 32) {
+            float4 a = R4[g];
+            a.x = e_of(a.x, invT, m); a.y = e_of(a.y, invT, m); a.z = e_of(a.z, invT, m); a.w = e_of(a.w, invT, m);
+            kahan(s, cc, a.x); kahan(s, cc, a.y); kahan(s, cc, a.z); kahan(s, cc, a.w);
+            R4[g] = a;
+            if (g == (x_first >> 2)) sm.rx[k & 1] = pick4(a, x_first & 3);
+        }
+        float Sh = s, Sl = -cc;
+        int kr = k;                          // the slot of R's warp partials and of rx
+        walk_sum(sm, k++, Sh, Sl);
+        bool sums_valid = true;
+        // children in input order: u+1, sub_end[u+1], ... below sub_end[u]
+        int nrej = 0;
+        int accepted = -1;
+        for (int c = c_first; !NAIVE && c >= 0 && c < se_u; c = sm.sub_end[c]) {
+            const float qx = sm.cq[c];
+            if (!isfinite(qx)) { nonfinite = 1; break; }
+            const float Sf = Sh + Sl;
+            float a = 1.f;
+            if (qx > 0.f) a = fminf(1.f, sm.rx[kr & 1] / (Sf * qx));
+            const float uc = sm.cu[c];
+            if (tid == 0 && fabsf(uc - a) < (float)kLowMargin) ++sm.lowm;
+            if (uc <= a) { accepted = c; break; }
+            // rejection: R' = max(0, R - S q_c), S' = sum R'; R' at the next child's token
+            const float4 *q4 = reinterpret_cast<const float4 *>(ssm + ((size_t)b * NQ + sm.qrow[c]) * V);
+            const int c_next = sm.sub_end[c] < se_u ? sm.sub_end[c] : -1;
+            const int x_next = c_next >= 0 ? sm.tok[c_next] : -1;
+            float s2 = 0.f, c2 = 0.f;
+            int bad = 0;
+            for (int g00 = g0 + lane; g00 < g1; g00 += 4 * 32) {
+                float4 qv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (g00 + 32 * j < g1) qv[j] = __ldg(q4 + g00 + 32 * j);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int g = g00 + 32 * j;
+                    if (g < g1) {
+                        bad |= !isfinite(qv[j].x) | !isfinite(qv[j].y) | !isfinite(qv[j].z) | !isfinite(qv[j].w);
+                        float4 r = R4[g];
+                        r.x = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].x, r.x));
+                        r.y = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].y, r.y));
+                        r.z = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].z, r.z));
+                        r.w = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].w, r.w));
+                        R4[g] = r;
+                        kahan(s2, c2, r.x); kahan(s2, c2, r.y); kahan(s2, c2, r.z); kahan(s2, c2, r.w);
+                        if (g == (x_next >> 2)) sm.rx[k & 1] = pick4(r, x_next & 3);
+                    }
+                }
+            }
+            // one reduction for both: a non-finite drafter value makes the sum NaN
+            float Nh = bad ? NAN : s2, Nl = bad ? 0.f : -c2;
+            const int kn = k;
+            walk_sum(sm, k++, Nh, Nl);
+            if (isnan(Nh)) { nonfinite = 1; break; }
+            if (Nh > 0.f) {
+                if (tid == 0) {
+                    sm.rej_q[nrej] = reinterpret_cast<const float *>(q4);
+                    sm.rej_S[nrej] = Sf;
+                }
+                ++nrej;
+                Sh = Nh;
+                Sl = Nl;
+                kr = kn;
+                sums_valid = true;
+            } else {
+                // zero normaliser: keep the residual unchanged (rebuilt from the
+                // rejections applied so far: the in-place pass overwrote it)
+                if (tid == 0) flag(status, TS_STATUS_ZERO_RESID);
+                const Resid keep{row, invT, m, sm.rej_q, sm.rej_S, nrej, nullptr};
+                for (int g = g0 + lane; g < g1; g += 32)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float v = resid_recompute(keep, 4 * g + e);
+                        R[4 * g + e] = v;
+                        if (4 * g + e == x_next) sm.rx[kn & 1] = v;
+                    }
+                __syncthreads();
+                kr = kn;
+                sums_valid = false;
+            }
+        }
+        if (nonfinite) break;
+        if (accepted >= 0) {
+            if (tid == 0) {
+                ot[cnt] = sm.tok[accepted];
+                op[cnt + 1] = sm.perm[accepted];
+            }
+            ++cnt;
+            u = accepted;
+            continue;
+        }
+        // ---- inverse CDF of the residual: the first y with C(y) > u * S
+        if (!sums_valid) {   // partials of the rebuilt residual
+            float s3 = 0.f, c3 = 0.f;
+            for (int g = g0 + lane; g < g1; g += 32) {
+                const float4 r = R4[g];
+                kahan(s3, c3, r.x); kahan(s3, c3, r.y); kahan(s3, c3, r.z); kahan(s3, c3, r.w);
+            }
+            float h3 = s3, l3 = -c3;
+            kr = k;
+            walk_sum(sm, k++, h3, l3);
+        }
+        // the warps' partial sums (lane l holds warp l's): inclusive scan, total,
+        // target = u * total, and the warp whose chunk holds it
+        const float oh = sm.red_hi[kr & 1][lane], ol = sm.red_lo[kr & 1][lane];
+        float ih = oh, il = ol;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float bh = __shfl_up_sync(0xffffffffu, ih, o), bl = __shfl_up_sync(0xffffffffu, il, o);
+            if (lane >= o) ff_add(ih, il, bh, bl);
+        }
+        const float toth = __shfl_sync(0xffffffffu, ih, 31), totl = __shfl_sync(0xffffffffu, il, 31);
+        float tgh, tgl;
+        ff_mul_f(toth, totl, sm.us, tgh, tgl);
+        const unsigned hitw = __ballot_sync(0xffffffffu, oh > 0.f && ff_gt(ih, il, tgh, tgl));
+        const unsigned posw = __ballot_sync(0xffffffffu, oh > 0.f);
+        int ws = hitw ? __ffs(hitw) - 1 : (posw ? 31 - __clz(posw) : 0);
+        const bool fallback = hitw == 0;
+        if (warp == ws) {
+            // this warp's exclusive prefix
+            float bh = __shfl_sync(0xffffffffu, ih, ws), bl = __shfl_sync(0xffffffffu, il, ws);
+            ff_add(bh, bl, -__shfl_sync(0xffffffffu, oh, ws), -__shfl_sync(0xffffffffu, ol, ws));
+            // lane j sums the float4s [g0 + j K, g0 + (j + 1) K) of the chunk
+            const int K = (g1 - g0 + 31) / 32;
+            const int a0 = min(g1, g0 + lane * K), a1 = min(g1, a0 + K);
+            float lh = 0.f, ll = 0.f;
+            for (int g = a0; g < a1; ++g) {
+                const float4 r = R4[g];
+                ff_add(lh, ll, r.x, 0.f); ff_add(lh, ll, r.y, 0.f); ff_add(lh, ll, r.z, 0.f); ff_add(lh, ll, r.w, 0.f);
+            }
+            float jh = lh, jl = ll;   // inclusive scan over the lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float xh = __shfl_up_sync(0xffffffffu, jh, o), xl = __shfl_up_sync(0xffffffffu, jl, o);
+                if (lane >= o) ff_add(jh, jl, xh, xl);
+            }
+            float ch = bh, cl = bl;   // C before this lane's range
+            ff_add(ch, cl, jh, jl);
+            ff_add(ch, cl, -lh, -ll);
+            float eh = bh, el = bl;   // C after it
+            ff_add(eh, el, jh, jl);
+            const unsigned hitl = fallback ? 0u : __ballot_sync(0xffffffffu, lh > 0.f && ff_gt(eh, el, tgh, tgl));
+            const unsigned posl = __ballot_sync(0xffffffffu, lh > 0.f);
+            const int wl = hitl ? __ffs(hitl) - 1 : (posl ? 31 - __clz(posl) : -1);
+            if (lane == wl) {
+                int chosen = -1, last_pos = -1;
+                float margin = 0.f;
+                for (int y = 4 * a0; y < 4 * a1 && chosen < 0; ++y) {
+                    const float r = R[y];
+                    if (r > 0.f) {
+                        float nh = ch, nl = cl;
+                        ff_add(nh, nl, r, 0.f);
+                        if (hitl && ff_gt(nh, nl, tgh, tgl)) {
+                            chosen = y;
+                            float d1h = tgh, d1l = tgl, d2h = nh, d2l = nl;
+                            ff_add(d1h, d1l, -ch, -cl);
+                            ff_add(d2h, d2l, -tgh, -tgl);
+                            margin = fminf(d1h + d1l, d2h + d2l) / toth;
+                        }
+                        last_pos = y;
+                        ch = nh;
+                        cl = nl;
+                    }
+                }
+                if (chosen < 0) chosen = last_pos;   // rounding left no bracket: the last token with mass
+                sm.chosen = chosen;
+                if (!(margin >= (float)kLowMargin)) ++sm.lowm;
+            } else if (wl < 0 && lane == 0) {
+                sm.chosen = 0;   // no mass anywhere (not reachable with S > 0)
+                ++sm.lowm;
+            }
+        }
+        __syncthreads();
+        const int chosen = sm.chosen;
+        if (tid == 0) ot[cnt] = chosen;
+        ++cnt;
+        if (!NAIVE) break;
+        // naive sampling: continue at the first child holding the drawn token
+        int next = -1;
+        for (int c = u + 1; c < se_u; c = sm.sub_end[c])
+            if (sm.tok[c] == chosen) { next = c; break; }
+        if (next < 0) break;
+        if (tid == 0) op[cnt] = sm.perm[next];
+        u = next;
+        __syncthreads();   // sm.chosen is rewritten at the next node
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (timeout) {
+            // the row copy may still be in flight: wait for it (bounded) before exiting
+            mbar_wait_bounded(bar, (visit - 1) & 1u);
+            out_count[b] = 0;
+            flag(status, TS_STATUS_TIMEOUT);
+        } else if (nonfinite) {
+            out_count[b] = 0;
+            flag(status, TS_STATUS_NONFINITE);
+        } else {
+            out_count[b] = cnt;
+        }
+        if (out_lowmargin) out_lowmargin[b] = sm.lowm;
+    }
+}
+
 }  // namespace
 
 size_t greedy_ws_bytes(int B, int n_max, int V) {
@@ -731,6 +1153,15 @@ cudaError_t launch_walk(int32_t *out_tokens, int32_t *out_path, int32_t *out_cou
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // the fast form: rows by bulk copy (V a multiple of 4, 16-byte aligned rows)
+    const size_t walk_smem = kWalkHeader + (size_t)V * sizeof(float);
+    const bool aligned = ((uintptr_t)logits & 15u) == 0 && (NAIVE || ((uintptr_t)ssm & 15u) == 0);
+    if (V % 4 == 0 && aligned && walk_smem <= (size_t)optin) {
+        cudaError_t e = cudaFuncSetAttribute(k_walk<NAIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)walk_smem);
+        if (e != cudaSuccess) return e;
+        return launch(k_walk<NAIVE>, dim3(t.B), dim3(kWalkThreads), walk_smem, s, out_tokens, out_path, out_count,
+                      out_lowmargin, logits, p_row, NP, ssm, q_row, NQ, uniforms, 1.0f / temperature, t, V, status);
+    }
     const size_t with_row = kMssHeader + (size_t)((V + 3) & ~3) * sizeof(float);
     if (with_row <= (size_t)optin) {
         cudaError_t e =

@@ -22,9 +22,17 @@ def to_device(a: np.ndarray, device, bf16: bool = False) -> torch.Tensor:
 
 
 class DeviceStep:
-    def __init__(self, w: Workload, device="cuda", attention: bool = True):
+    """paged: keep the KV cache in pages of api.PAGE_KEYS rows (randomly placed,
+    listed per request in a block table) and run the paged calls.
+    serial_verify: run verification after the attention on the main stream
+    (the order a verification that also commits would need)."""
+
+    def __init__(self, w: Workload, device="cuda", attention: bool = True, paged: bool = False,
+                 serial_verify: bool = False, seed: int = 0):
         self.w = w
         self.device = device
+        self.paged = paged
+        self.serial_verify = serial_verify
         dev = device
         B, n_max = w.B, w.n_max
         i32 = lambda a: to_device(np.asarray(a, np.int32), dev)
@@ -64,10 +72,38 @@ class DeviceStep:
             self.q = to_device(w.q, dev, bf)
             self.k_new = to_device(w.k_new, dev, bf)
             self.v_new = to_device(w.v_new, dev, bf)
-            self.k_cache = to_device(w.k_cache, dev, bf)
-            self.v_cache = to_device(w.v_cache, dev, bf)
             self.out = torch.zeros_like(self.q)
             self.ws_attn = api.workspace(api.TS_OP_ATTENTION, B, w.H, n_max, w.d, w.L_max, w.V, device=dev)
+            if paged:
+                self.kv = self._pages(np.random.default_rng(seed))
+                self.k_cache = self.v_cache = None
+                self._fused = False
+            else:
+                self.k_cache = to_device(w.k_cache, dev, bf)
+                self.v_cache = to_device(w.v_cache, dev, bf)
+
+    def _pages(self, rng):
+        """The prefix cache scattered into randomly placed pages of PAGE_KEYS rows."""
+        w, PK = self.w, api.PAGE_KEYS
+        if w.dtype != "bf16":
+            raise ValueError("the paged cache holds bf16 rows")
+        max_pages = (w.L_max + PK - 1) // PK
+        need = [(int(w.prefix_len[b]) + w.n_max + PK - 1) // PK for b in range(w.B)]
+        ids = rng.permutation(sum(need))
+        bt = np.full((w.B, max_pages), -1, np.int32)
+        kp = np.zeros((len(ids), w.H, PK, w.d), np.uint16)
+        vp = np.zeros_like(kp)
+        nxt = 0
+        for b in range(w.B):
+            for j in range(need[b]):
+                g = int(ids[nxt])
+                nxt += 1
+                bt[b, j] = g
+                lo, hi = j * PK, min((j + 1) * PK, w.L_max)
+                kp[g, :, :hi - lo] = w.k_cache[b, :, lo:hi]
+                vp[g, :, :hi - lo] = w.v_cache[b, :, lo:hi]
+        dv = self.device
+        return api.PagedKV(to_device(kp, dv, True), to_device(vp, dv, True), to_device(bt, dv))
 
     # -- the five rows of the hot path ----------------------------------------
     def build(self, stream=None):
@@ -83,10 +119,17 @@ class DeviceStep:
                            status=self.status, stream=stream)
 
     def append(self, stream=None):
+        if self.paged:
+            api.kv_append_paged(self.kv, self.k_new, self.v_new, self.prefix_len, self.tree, self.status, stream)
+            return
         api.kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.prefix_len, self.tree, self.status,
                       stream)
 
     def attend(self, stream=None):
+        if self.paged:
+            api.tree_attention_paged(self.out, self.q, self.kv, self.prefix_len, self.tree, 0.0, self.ws_attn,
+                                     self.status, stream)
+            return
         api.tree_attention(self.out, self.q, self.k_cache, self.v_cache, self.prefix_len, self.tree, 0.0,
                            self.ws_attn, self.status, stream)
 
@@ -108,6 +151,10 @@ class DeviceStep:
         kind = kind or self.w.verify
         path, count = ((self.mss_path, self.mss_count) if kind in ("mss", "both", "naive")
                        else (self.out_path, self.out_count))
+        if self.paged:
+            api.kv_commit_paged(self.kv, self.prefix_len, self.new_prefix_len, path, count, self.tree, self.status,
+                                stream)
+            return
         api.kv_commit(self.k_cache, self.v_cache, self.prefix_len, self.new_prefix_len, path, count, self.tree,
                       self.status, stream)
 
@@ -119,6 +166,13 @@ class DeviceStep:
         if not self.attention:
             self.build(main)
             self.verify(kind, main)
+            return
+        if self.serial_verify:   # one stream: build, append, attention, verification, commit
+            self.build(main)
+            self.append(main)
+            self.attend(main)
+            self.verify(kind, main)
+            self.commit(kind, main)
             return
         if self._side is None:
             self._side = torch.cuda.Stream(self.device)

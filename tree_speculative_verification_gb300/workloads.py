@@ -154,18 +154,25 @@ def _round_up(x, m):
     return (x + m - 1) // m * m
 
 
-def make(name: str, seed: int | None = None, *, attention: bool = True, scale_down: int = 1) -> Workload:
+def make(name: str, seed: int | None = None, *, attention: bool = True, scale_down: int = 1,
+         batch: int | None = None) -> Workload:
     """Build one of the five workloads.
 
     name       : tiny | llama7b | merge | long65b | opt30b
     seed       : defaults to the workload's own seed (0..4)
     attention  : False skips Q/K/V (verification-only callers)
     scale_down : divides batch (and the long prefix) for reduced-size parity runs
+    batch      : the LLaMA-7B-shaped layer at another batch size (the other
+                 workloads keep theirs)
     """
     seeds = dict(tiny=0, llama7b=1, merge=2, long65b=3, opt30b=4)
     if name not in seeds:
         raise ValueError(f"unknown workload {name!r}; choose from {CONFIG_NAMES}")
     rng = np.random.default_rng(seeds[name] if seed is None else seed)
+    if batch is not None:
+        if name != "llama7b":
+            raise ValueError("batch overrides only the llama7b workload")
+        return _make_llama7b(rng, attention, 1, batch=int(batch))
     return globals()["_make_" + name](rng, attention, max(1, int(scale_down)))
 
 
@@ -240,11 +247,11 @@ def _make_tiny(rng, attention, sd):
                                verify="both", attention=attention)
 
 
-def _make_llama7b(rng, attention, sd):
+def _make_llama7b(rng, attention, sd, batch=None):
     """LLaMA-7B-shaped layer: batch 8, 32 heads x 128, bf16, prefix 2048,
     widths (1,1,3,1,1,1,1,1) -> 21 nodes; greedy, vocab 32000, logits N(0, 3^2);
     first child planted as the target argmax with probability 0.68."""
-    return _expansion_workload(rng, name="llama7b", B=max(1, 8 // sd), H=32, d=128, dtype="bf16", P=2048,
+    return _expansion_workload(rng, name="llama7b", B=batch or max(1, 8 // sd), H=32, d=128, dtype="bf16", P=2048,
                                widths=(1, 1, 3, 1, 1, 1, 1, 1), V=32000, sigma_t=3.0, sigma_noise=0.0,
                                independent_ssm=False, plant=0.68, verify="greedy", attention=attention)
 
