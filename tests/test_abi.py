@@ -139,6 +139,17 @@ def test_kernel_choice(lib, n_max, d, expect, monkeypatch):
     assert api.attention_kernel(8, 32, n_max, d, 2048 + n_max, api.TS_F32) == "k_attn_f32"
 
 
+@pytest.mark.parametrize("B,expect", [(1, "k_attn_tq"), (4, "k_attn_tq"), (5, "k_attn_bf16<"), (8, "k_attn_bf16<"),
+                                      (9, "k_attn_bf16<"), (10, "k_attn_tq"), (16, "k_attn_tq")])
+def test_kernel_choice_small_trees_by_batch(lib, B, expect, monkeypatch):
+    """Trees of up to 32 nodes at head_dim 128 (32 heads, 152 SMs when no GPU
+    is present): the mma.sync kernel only when the (request, head) pairs fill
+    one wave of its two CTAs per SM, 152 < B*H <= 304."""
+    for var in ("TREESPEC_ATTN_KERNEL", "TREESPEC_ATTN_SPLITS"):
+        monkeypatch.delenv(var, raising=False)
+    assert api.attention_kernel(B, 32, 21, 128, 2048 + 21, api.TS_BF16).startswith(expect)
+
+
 @pytest.mark.parametrize("force,n_max,expect", [("mma", 47, "k_attn_bf16<"), ("tq", 21, "k_attn_tq"),
                                                  ("mma", 21, "k_attn_bf16<")])
 def test_kernel_override(lib, force, n_max, expect, monkeypatch):

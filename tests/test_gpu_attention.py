@@ -87,6 +87,7 @@ def test_bf16_every_variant(n_max, monkeypatch):
 
 @pytest.mark.parametrize("splits", ["1", "2", "5", "64"])
 def test_bf16_forced_splits_ragged(splits, monkeypatch):
+    monkeypatch.setenv("TREESPEC_ATTN_KERNEL", "mma")   # the split-KV kernel
     monkeypatch.setenv("TREESPEC_ATTN_SPLITS", splits)
     rng = np.random.default_rng(100 + int(splits))
     B, H, n_max = 4, 2, 21

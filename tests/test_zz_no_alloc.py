@@ -28,11 +28,11 @@ def _inputs(rng, B, H, d, n, L_max):
     return q, kn, vn, kc, vc
 
 
-# (widths, plan): the LLaMA-7B-shaped expansion tree (21 nodes) on few heads, so
-# the mma.sync kernel splits the key axis and its partials really go to the
-# scratch; the OPT-30B-shaped tree (47 nodes), for which the persistent tcgen05
-# kernel keeps its item queue in the scratch
-CASES = [((1, 1, 3, 1, 1, 1, 1, 1), "k_attn_bf16<"), ((2, 2, 2, 2, 1), "k_attn_tq")]
+# (widths, kernel): the LLaMA-7B-shaped expansion tree (21 nodes) on few heads
+# with the mma.sync kernel, which then splits the key axis so that its partials
+# really go to the scratch; the OPT-30B-shaped (47 nodes) and the 21-node tree
+# with the persistent tcgen05 kernel, which keeps its item queue in the scratch
+CASES = [((1, 1, 3, 1, 1, 1, 1, 1), "k_attn_bf16<"), ((2, 2, 2, 2, 1), "k_attn_tq"), ((1, 1, 3, 1, 1, 1, 1, 1), "k_attn_tq")]
 
 
 @pytest.mark.parametrize("widths,kernel", CASES)
@@ -42,6 +42,7 @@ def test_noalloc_matches_workspace_entry_point_twice(widths, kernel, monkeypatch
     call must not see what the first left in the scratch)."""
     for var in ("TREESPEC_ATTN_KERNEL", "TREESPEC_ATTN_SPLITS"):
         monkeypatch.delenv(var, raising=False)
+    monkeypatch.setenv("TREESPEC_ATTN_KERNEL", "mma" if kernel.startswith("k_attn_bf16") else "tq")
     lib = api.load_library()
     B, H, d, L_max = 2, 4, 128, 1600
     n = 1

@@ -608,17 +608,23 @@ Variant pick(int n_max) {
 }
 
 // Kernel choice for head_dim 128: trees of 33..128 nodes go to the persistent
-// 128-key-tile tcgen05 kernel (k_attn_tq, attn_tq.cu), all others (and
-// head_dim 64) to the mma.sync kernel. TREESPEC_ATTN_KERNEL=mma or tq forces
-// one of them where its limits allow. Measured on GB300: k_attn_tq on a
-// 21-node tree over a 2048-key prefix (batch 8, 32 heads) 52.8 us against
-// 51.2 us for the mma.sync kernel (256 whole-pair items on 152 persistent CTAs
-// leave 104 CTAs with two items and 48 with one).
-bool use_tq(int d, int n_max) {
+// 128-key-tile tcgen05 kernel (k_attn_tq, attn_tq.cu). Smaller trees go to it
+// too, except when the (request, head) pairs fill exactly one wave of the
+// mma.sync kernel's two CTAs per SM (SMs < pairs <= 2 SMs). Measured on GB300
+// for 21-node trees over a 2048-key prefix (32 heads): batch 4 (128 pairs)
+// tcgen05 29.6 us vs mma.sync 50.4 us (which must split keys to fill the
+// SMs); batch 8 (256 pairs) 53.7 vs 51.4 us; batch 16 (512 pairs) 98.9 vs
+// 96.9 us; merged-chain trees over ragged prefixes (512 pairs) 113.0 vs
+// 117.4 us (the persistent kernel's queue balances the ragged items). Head
+// dim 64 and trees of more than 128 nodes: the mma.sync kernel.
+// TREESPEC_ATTN_KERNEL=mma or tq forces one of them where its limits allow.
+bool use_tq(int d, int n_max, long long pairs) {
     if (d != 128 || n_max > 128) return false;
     const char *e = getenv("TREESPEC_ATTN_KERNEL");
     if (e && *e) return strcmp(e, "tq") == 0;
-    return n_max > 32;
+    if (n_max > 32) return true;
+    const long long sms = num_sms();
+    return !(pairs > sms && pairs <= 2 * sms);
 }
 
 Variant pick_variant(int d, int n_max) { return d == 64 ? pick<64>(n_max) : pick<128>(n_max); }
@@ -647,7 +653,7 @@ int num_sms() {
 AttnPlan attn_plan(int B, int H, int n_max, int d, int L_max, ts_dtype dt) {
     AttnPlan p{1, 1, 0, 0, "k_attn_f32"};
     if (dt != TS_BF16) return p;
-    if (use_tq(d, n_max)) {
+    if (use_tq(d, n_max, (long long)B * H)) {
         p.tq = true;
         p.n_pad = 128;
         p.kernel = "k_attn_tq";
