@@ -7,10 +7,10 @@
 // causal mask of sec. 4.2, a bit test on the ancestor bitmask).
 //
 // GB300 design. Each CTA (one per SM) walks (request, head) items: its first
-// item is blockIdx.x, every later one is taken from a queue in the workspace
-// (gridDim.x + an atomic counter), so that CTAs which start late -- their SM
-// still held by a kernel of another stream -- take fewer items instead of
-// finishing last. The K/V ring, the two score buffers and the softmax run on
+// item is the blockIdx.x-th, every later one is taken from a queue in the
+// workspace (gridDim.x + an atomic counter), so that CTAs which start late --
+// their SM still held by a kernel of another stream -- take fewer items
+// instead of finishing last. Items are handed out longest request first. The K/V ring, the two score buffers and the softmax run on
 // across item boundaries.
 //   warp 0    TMA producer and item queue (lane 0): claims the next item one
 //             item ahead and publishes it in a 4-slot shared-memory ring
@@ -67,7 +67,8 @@ struct TqCfg {
     static constexpr int OFF_REQ = OFF_XO + 4 * 32 * XO_STRIDE * 4;
     static constexpr int RING = 4;                        // published items (the queue's shared-memory ring)
     static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 2 * RING;
-    static constexpr int OFF_BAR = OFF_REQ + REQ_CACHE * 8;
+    static constexpr int OFF_ORDER = OFF_REQ + REQ_CACHE * 8;   // requests longest first
+    static constexpr int OFF_BAR = OFF_ORDER + REQ_CACHE * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     // misc ints: [0] TMEM base, [1] timeout, [4..8) item ring, [8..24) the softmax
     // warps' votes on a ring slot (two sets of eight)
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     float *mx_s = (float *)(sm + C::OFF_MX);
     float *ls_s = (float *)(sm + C::OFF_LS);
     int2 *req_s = (int2 *)(sm + C::OFF_REQ);
+    int *order_s = (int *)(sm + C::OFF_ORDER);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pairs = a.t.B * a.H, G = gridDim.x;
@@ -231,6 +233,20 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     }
     // every role reads the requests' (n, P) at each item: one copy in shared memory
     for (int b = tid; b < a.t.B && b < C::REQ_CACHE; b += C::THREADS) req_s[b] = make_int2(a.t.n_nodes[b], a.prefix_len[b]);
+    __syncthreads();
+    // the producer hands out the requests' items longest first (keys P + n,
+    // ties to the lower request), so that with ragged prefixes the last items
+    // of the launch are short ones; request order when B exceeds the cache
+    const bool lpt = a.t.B <= C::REQ_CACHE;
+    for (int b = tid; lpt && b < a.t.B; b += C::THREADS) {
+        const int kb = req_s[b].x > 0 ? req_s[b].x + req_s[b].y : -1;
+        int rank = 0;
+        for (int o = 0; o < a.t.B; ++o) {
+            const int ko = req_s[o].x > 0 ? req_s[o].x + req_s[o].y : -1;
+            rank += ko > kb || (ko == kb && o < b);
+        }
+        order_s[rank] = b;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -241,8 +257,9 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             // the next item with key tiles (the first: blockIdx.x; later ones
             // gridDim.x + the queue counter), -1 when none is left
             auto claim = [&](bool first) -> int {
-                for (int p = first ? (int)blockIdx.x : G + (int)atomicAdd(&a.counters[0], 1u); p < pairs;
-                     p = G + (int)atomicAdd(&a.counters[0], 1u)) {
+                for (int q = first ? (int)blockIdx.x : G + (int)atomicAdd(&a.counters[0], 1u); q < pairs;
+                     q = G + (int)atomicAdd(&a.counters[0], 1u)) {
+                    const int p = lpt ? order_s[q / a.H] * a.H + q % a.H : q;   // the q-th item, longest first
                     const TqItem it = tq_item(a, req_s, p);
                     if (it.ntiles > 0) return p;
                     if (it.n > 0 && it.h == 0) flag(a.status, TS_STATUS_INDEX);
