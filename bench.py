@@ -408,6 +408,7 @@ def measure_other_config(name, args, device, stream):
     line = {"value": nodes / (out["step"] * 1e-3), "unit": "nodes/s", "ms_per_step": out["step"],
             "nodes_per_step": nodes, "attention_ms": out["attend"], "verify_ms": out["verify"], "verify": kind,
             "attention_kernel": kernel, "roofline_frac": roof["frac"], "attention_gbs": roof["achieved"],
+            "attention_traffic_bytes": roof["traffic"],
             "accepted_tokens_per_step": s.accepted(kind), "steps": K, "workload": DESCR[name]}
     del s, w
     torch.cuda.synchronize()
