@@ -6,11 +6,13 @@
 // prefix key and the tree keys of its ancestors and itself (the topology-aware
 // causal mask of sec. 4.2, a bit test on the ancestor bitmask).
 //
-// GB300 design. Each CTA (one per SM) walks (request, head) items: its first
-// item is the blockIdx.x-th, every later one is taken from a queue in the
-// workspace (gridDim.x + an atomic counter), so that CTAs which start late --
-// their SM still held by a kernel of another stream -- take fewer items
-// instead of finishing last. Items are handed out longest request first. The K/V ring, the two score buffers and the softmax run on
+// GB300 design. Each CTA (one per SM) walks (request, head) items taken from a
+// queue in the workspace (an atomic counter), its first item included, so that
+// CTAs which start late -- their SM still held by a kernel of another stream --
+// take fewer and shorter items instead of holding a long one to the end (a
+// fixed first item per CTA made the merge-workload step, whose sampling walk
+// holds 16 SMs, 131 us instead of 119 us). Items are handed out longest
+// request first. The K/V ring, the two score buffers and the softmax run on
 // across item boundaries.
 //   warp 0    TMA producer and item queue (lane 0): claims the next item one
 //             item ahead and publishes it in a 4-slot shared-memory ring
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     int *order_s = (int *)(sm + C::OFF_ORDER);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pairs = a.t.B * a.H, G = gridDim.x;
+    const int pairs = a.t.B * a.H;
     pdl_wait();
     pdl_trigger();
 
@@ -254,11 +256,9 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
 
     if (warp == 0) {
         if (lane == 0) {   // ---------------------------------------------- TMA producer, item queue
-            // the next item with key tiles (the first: blockIdx.x; later ones
-            // gridDim.x + the queue counter), -1 when none is left
-            auto claim = [&](bool first) -> int {
-                for (int q = first ? (int)blockIdx.x : G + (int)atomicAdd(&a.counters[0], 1u); q < pairs;
-                     q = G + (int)atomicAdd(&a.counters[0], 1u)) {
+            // the next item with key tiles from the queue, -1 when none is left
+            auto claim = [&]() -> int {
+                for (int q = (int)atomicAdd(&a.counters[0], 1u); q < pairs; q = (int)atomicAdd(&a.counters[0], 1u)) {
                     const int p = lpt ? order_s[q / a.H] * a.H + q % a.H : q;   // the q-th item, longest first
                     const TqItem it = tq_item(a, req_s, p);
                     if (it.ntiles > 0) return p;
@@ -276,10 +276,10 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                 return true;
             };
             int g = 0, k = 0;
-            int p = claim(true);
+            int p = claim();
             bool ok = publish(0, p);
             while (ok && p >= 0) {
-                const int pn = claim(false);   // published before this item's tiles: readers see it an item early
+                const int pn = claim();   // published before this item's tiles: readers see it an item early
                 if (!publish(k + 1, pn)) {
                     ok = false;
                     break;
@@ -696,7 +696,7 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     a.chunk_tiles = 0;
     a.splits = 1;
     a.n_pad = TqCfg::NODES;
-    a.counters = queue;   // [0] next item - gridDim.x, [1] CTAs finished
+    a.counters = queue;   // [0] next item, [1] CTAs finished
     a.part_ml = nullptr;
     a.part_o = nullptr;
     a.status = status;

@@ -698,26 +698,38 @@ __global__ void __launch_bounds__(kMssThreads, 1) k_mss(int32_t *out_tokens, int
 //  * warp w owns the contiguous float4 range [w C4, (w + 1) C4) of the
 //    vocabulary in every pass (lane-consecutive 16-byte shared-memory accesses,
 //    no bank conflicts), so the per-warp partial sums of a pass are also the
-//    coarse level of the inverse CDF;
-//  * the visited node's target row arrives by bulk copy (TMA engine) into the
-//    residual buffer R, completing on an mbarrier;
-//  * block reductions are float-float: every warp writes its partial, one
-//    barrier, and every warp combines the 32 partials itself (identical
-//    results: the butterfly and the float-float add are symmetric), into
-//    double-buffered slots, so each reduction costs one barrier;
-//  * a child's test needs no barrier: the pass before it records R at the
-//    child's token (double-buffered), and every warp takes the same verdict.
-// Elementwise arithmetic is the same fp32 as k_mss; sums are compensated fp32
-// per thread, float-float across threads; ratio and CDF tests in fp32 /
-// float-float (no fp64 in per-thread code: GB300's fp64 rate is low).
+//    coarse level of the inverse CDF, and no warp ever touches another's range;
+//  * each warp's range of the visited node's target row arrives by its own
+//    bulk copy (TMA engine) into the residual buffer R, on the warp's own
+//    mbarrier, and the warp takes its maximum, its exponentials relative to
+//    that maximum and their sum as soon as its range has landed. R stays
+//    relative to its warp's maximum (factor f_w to the row maximum) until the
+//    first rejection pass rescales it; the tests and the final sample apply
+//    f_w where it still does;
+//  * a reduction is two barriers: every warp publishes its float-float
+//    partial, then warp 0 alone combines the 32 partials (row maximum, S),
+//    takes the child's test or the coarse level of the final sample, and
+//    publishes the verdict, which every warp reads after the second barrier.
+// Elementwise arithmetic is fp32 (the hardware exp2); sums are fp32 over a
+// float4, compensated across float4s, float-float across threads; ratio and
+// CDF tests in fp32 / float-float (no fp64 in per-thread code: GB300's fp64
+// rate is low).
 constexpr int kWalkThreads = 1024;
 constexpr int kWalkWarps = kWalkThreads / 32;
-constexpr uint32_t kBulkChunk = 32768;
+
+// Verdicts of the deciding warp (a child index >= 0: that child is accepted)
+constexpr int kVReject = -1;      // the tested child is rejected: its rejection pass follows
+constexpr int kVSample = -2;      // no child left to test: the final sample follows
+constexpr int kVZero = -3;        // the rejection left a zero normaliser: the residual is rebuilt
+constexpr int kVNonfinite = -4;   // a non-finite target or drafter value
+constexpr int kVTimeout = -5;     // a row copy did not complete
 
 struct WalkShared {
-    float red_mx[2][kWalkWarps];
-    float red_hi[2][kWalkWarps], red_lo[2][kWalkWarps];
-    int red_bad[2][kWalkWarps];
+    float red_mx[kWalkWarps];               // the warps' published partials
+    float red_hi[kWalkWarps], red_lo[kWalkWarps];
+    int red_bad[kWalkWarps];
+    int bad[kWalkWarps];                    // the warps' index checks
+    float f[kWalkWarps];                    // each warp's factor to the row maximum
     float cq[kMaxNodes];                    // q_c(x_c) of each child of the current node
     float cu[kMaxNodes];                    // its accept uniform
     int depth[kMaxNodes];
@@ -728,17 +740,22 @@ struct WalkShared {
     int qrow[kMaxNodes];
     const float *rej_q[kMaxNodes];
     float rej_S[kMaxNodes];
-    float rx[2];                            // R at the token of the next child to test
+    float Sh, Sl;                           // the current normaliser S (float-float)
+    float m;                                // the row's tempered maximum (natural units)
+    float rx;                               // R at the token of the child tested next
     float us;                               // the final-sample uniform of the current node
+    int nrej;                               // rejections applied to the current residual
+    int verdict;
     int chosen;
     int lowm;
-    unsigned long long bar;                 // completion of the row's bulk copy
+    // the final sample's coarse level: the warp whose range holds the target,
+    // whether rounding left no bracket, the warp's exclusive prefix, the target
+    // u * total (float-float) and the total
+    int ws, fb;
+    float bh, bl, tgh, tgl, toth;
+    unsigned long long wbar[kWalkWarps];    // completion of each warp's bulk copy of its range
 };
 constexpr size_t kWalkHeader = (sizeof(WalkShared) + 127) & ~(size_t)127;
-
-__device__ __forceinline__ float pick4(const float4 &a, int e) {
-    return e == 0 ? a.x : (e == 1 ? a.y : (e == 2 ? a.z : a.w));
-}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -767,33 +784,136 @@ __device__ __forceinline__ void ff_mul_f(float h, float l, float x, float &oh, f
     ol = e - (oh - p);
 }
 
-// Block maximum (and OR of a flag), the same in every warp; one barrier.
-__device__ float walk_max(WalkShared &sm, int k, float x, int flag_in, int &flag_out) {
+// A warp's partial of a reduction into its slots: its float-float sum (h, l),
+// its maximum mx and the OR of its flags. The block barrier follows.
+__device__ __forceinline__ void walk_publish(WalkShared &sm, float h, float l, float mx, int flag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    x = warp_max(x);
-    flag_in = __any_sync(0xffffffffu, flag_in);
+    warp_ff_sum(h, l);
+    flag = __reduce_or_sync(0xffffffffu, flag);
     if (lane == 0) {
-        sm.red_mx[k & 1][warp] = x;
-        sm.red_bad[k & 1][warp] = flag_in;
+        sm.red_hi[warp] = h;
+        sm.red_lo[warp] = l;
+        sm.red_mx[warp] = mx;
+        sm.red_bad[warp] = flag;
     }
-    __syncthreads();
-    flag_out = __any_sync(0xffffffffu, sm.red_bad[k & 1][lane]);
-    return warp_max(sm.red_mx[k & 1][lane]);
 }
 
-// Block float-float sum, the same in every warp; the warps' partials stay in
-// slot k & 1 (the coarse level of the inverse CDF). One barrier.
-__device__ void walk_sum(WalkShared &sm, int k, float &h, float &l) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// The test of child c (Algorithm 2: accept with probability
+// min(1, p(x_c) / q_c(x_c)), p = R / S), by lane 0 of the deciding warp;
+// kVSample when c is not a child of the current node.
+__device__ void walk_test(WalkShared &sm, int c, int se_u, bool local, int C4) {
+    if (c < 0 || c >= se_u) {
+        sm.verdict = kVSample;
+        return;
+    }
+    const float qx = sm.cq[c];
+    if (!isfinite(qx)) {
+        sm.verdict = kVNonfinite;
+        return;
+    }
+    const float Sf = sm.Sh + sm.Sl;
+    float rxv = sm.rx;
+    if (local) rxv *= sm.f[(sm.tok[c] >> 2) / C4];   // R relative to the maximum of the warp holding x_c
+    float a = 1.f;
+    if (qx > 0.f) a = fminf(1.f, rxv / (Sf * qx));
+    const float uc = sm.cu[c];
+    if (fabsf(uc - a) < (float)kLowMargin) ++sm.lowm;
+    sm.verdict = uc <= a ? c : kVReject;
+}
+
+// The deciding warp: the coarse level of the inverse CDF, from the warps'
+// partials (times f while R is relative to the warps' maxima): the first warp
+// whose inclusive prefix exceeds u * total.
+__device__ void walk_coarse(WalkShared &sm, bool local) {
+    const int lane = threadIdx.x & 31;
+    float oh = sm.red_hi[lane], ol = sm.red_lo[lane];
+    if (local) ff_mul_f(oh, ol, sm.f[lane], oh, ol);
+    float ih = oh, il = ol;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float bh = __shfl_up_sync(0xffffffffu, ih, o), bl = __shfl_up_sync(0xffffffffu, il, o);
+        if (lane >= o) ff_add(ih, il, bh, bl);
+    }
+    const float toth = __shfl_sync(0xffffffffu, ih, 31), totl = __shfl_sync(0xffffffffu, il, 31);
+    float tgh, tgl;
+    ff_mul_f(toth, totl, sm.us, tgh, tgl);
+    const unsigned hitw = __ballot_sync(0xffffffffu, oh > 0.f && ff_gt(ih, il, tgh, tgl));
+    const unsigned posw = __ballot_sync(0xffffffffu, oh > 0.f);
+    const int ws = hitw ? __ffs(hitw) - 1 : (posw ? 31 - __clz(posw) : 0);
+    float bh = __shfl_sync(0xffffffffu, ih, ws), bl = __shfl_sync(0xffffffffu, il, ws);
+    ff_add(bh, bl, -__shfl_sync(0xffffffffu, oh, ws), -__shfl_sync(0xffffffffu, ol, ws));
+    if (lane == 0) {
+        sm.ws = ws;
+        sm.fb = hitw == 0;
+        sm.bh = bh;
+        sm.bl = bl;
+        sm.tgh = tgh;
+        sm.tgl = tgl;
+        sm.toth = toth;
+    }
+}
+
+// The deciding warp after a node's statistics: the row maximum M (log2
+// units), f_w = 2^(M_w - M), S = sum_w S_w f_w, then the first child's test
+// (or the final sample's coarse level).
+__device__ void walk_decide_stats(WalkShared &sm, int c_first, int se_u, int C4, bool naive) {
+    const int lane = threadIdx.x & 31;
+    const int flags = __reduce_or_sync(0xffffffffu, sm.red_bad[lane]);
+    const float ml = sm.red_mx[lane];
+    const float M = warp_max(ml);
+    const float fl = exp2f(ml - M);   // 0 for a warp with an empty range (ml = -inf)
+    float h, l;
+    ff_mul_f(sm.red_hi[lane], sm.red_lo[lane], fl, h, l);
+    warp_ff_sum(h, l);
+    sm.f[lane] = fl;
+    __syncwarp();
+    if (lane == 0) {
+        sm.Sh = h;
+        sm.Sl = l;
+        sm.m = M * 0.6931471805599453f;
+        sm.nrej = 0;
+        if (flags & 2) sm.verdict = kVTimeout;
+        else if (flags & 1) sm.verdict = kVNonfinite;
+        else if (naive) sm.verdict = kVSample;
+        else walk_test(sm, c_first, se_u, true, C4);
+    }
+    __syncwarp();
+    if (sm.verdict == kVSample) walk_coarse(sm, true);
+}
+
+// The deciding warp after child c's rejection pass: S' = sum of the residual;
+// a NaN sum means a non-finite drafter value; S' > 0 records the rejection
+// and tests child c_next; S' = 0 asks for the residual to be rebuilt.
+__device__ void walk_decide_resid(WalkShared &sm, const float *q_c, int c_next, int se_u, int C4, uint32_t *status) {
+    const int lane = threadIdx.x & 31;
+    float h = sm.red_hi[lane], l = sm.red_lo[lane];
     warp_ff_sum(h, l);
     if (lane == 0) {
-        sm.red_hi[k & 1][warp] = h;
-        sm.red_lo[k & 1][warp] = l;
+        if (isnan(h)) {
+            sm.verdict = kVNonfinite;
+        } else if (h > 0.f) {
+            sm.rej_q[sm.nrej] = q_c;
+            sm.rej_S[sm.nrej] = sm.Sh + sm.Sl;
+            ++sm.nrej;
+            sm.Sh = h;
+            sm.Sl = l;
+            walk_test(sm, c_next, se_u, false, C4);
+        } else {
+            flag(status, TS_STATUS_ZERO_RESID);
+            sm.verdict = kVZero;
+        }
     }
-    __syncthreads();
-    h = sm.red_hi[k & 1][lane];
-    l = sm.red_lo[k & 1][lane];
-    warp_ff_sum(h, l);
+    __syncwarp();
+    if (sm.verdict == kVSample) walk_coarse(sm, false);
+}
+
+// The deciding warp after the residual was rebuilt (S unchanged): the test of
+// child c_next.
+__device__ void walk_decide_rebuilt(WalkShared &sm, int c_next, int se_u, int C4) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) walk_test(sm, c_next, se_u, false, C4);
+    __syncwarp();
+    if (sm.verdict == kVSample) walk_coarse(sm, false);
 }
 
 template <bool NAIVE>
@@ -807,7 +927,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
     float *R = reinterpret_cast<float *>(walk_smem + kWalkHeader);
     float4 *R4 = reinterpret_cast<float4 *>(R);
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t bar = smem_u32(&sm.bar);
+    const uint32_t wbar = smem_u32(&sm.wbar[warp]);
     pdl_wait();
     pdl_trigger();
     const int n = t.n_nodes[b];
@@ -823,7 +943,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
     }
     if (tid == 0) {
         sm.lowm = 0;
-        mbar_init(bar, 1);
+        for (int w = 0; w < kWalkWarps; ++w) mbar_init(smem_u32(&sm.wbar[w]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // tree and row indices into shared memory; index checks for every node
@@ -846,12 +966,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
             if (qr < 0 || qr >= NQ || sm.tok[i] < 0 || sm.tok[i] >= V) bad_index = 1;
         }
     }
-    // per-warp flags through a reduction slot that the walk's first use of it
-    // (an odd-numbered maximum) overwrites only behind later barriers
     bad_index = __any_sync(0xffffffffu, bad_index);
-    if (lane == 0) sm.red_bad[1][warp] = bad_index;
+    if (lane == 0) sm.bad[warp] = bad_index;
     __syncthreads();
-    if (__any_sync(0xffffffffu, sm.red_bad[1][lane])) {
+    if (__any_sync(0xffffffffu, sm.bad[lane])) {
         if (tid == 0) {
             out_count[b] = 0;
             if (out_lowmargin) out_lowmargin[b] = 0;
@@ -864,80 +982,94 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
     const int V4 = V >> 2;
     const int C4 = (V4 + kWalkWarps - 1) / kWalkWarps;          // float4s of a warp's chunk
     const int g0 = min(V4, warp * C4), g1 = min(V4, g0 + C4);     // this warp's chunk
+    const float a2 = invT * kL2E;
     int u = 0, cnt = 0, nonfinite = 0, timeout = 0;
-    int k = 0;            // reductions so far (slot parity)
     uint32_t visit = 0;   // bulk copies so far (mbarrier phase)
     if (tid == 0) op[0] = sm.perm[0];
 
     for (int step = 0; step < n; ++step) {
         const float *row = logits + ((size_t)b * NP + sm.prow[u]) * V;
         const int du = sm.depth[u], se_u = sm.sub_end[u];
-        // the node's row into R by bulk copy (every earlier access of R is
-        // behind the last barrier; the proxy fence orders them before the copy)
-        if (tid == 0) {
+        const int c_first = u + 1 < se_u ? u + 1 : -1;
+        // this warp's range of the node's row into R by bulk copy (the warp's
+        // earlier accesses of its range are behind the last barrier; the proxy
+        // fence orders them before the copy). An empty range completes at once.
+        if (lane == 0) {
             fence_async_smem();
-            mbar_expect_tx(bar, (uint32_t)V * 4u);
-            for (uint32_t off = 0; off < (uint32_t)V * 4u; off += kBulkChunk)
-                bulk_g2s(smem_u32(R) + off, (const char *)row + off, min(kBulkChunk, (uint32_t)V * 4u - off), bar);
+            mbar_expect_tx(wbar, (uint32_t)(g1 - g0) * 16u);
+            if (g1 > g0)
+                bulk_g2s(smem_u32(R4 + g0), reinterpret_cast<const float4 *>(row) + g0, (uint32_t)(g1 - g0) * 16u,
+                         wbar);
         }
-        // meanwhile: the values the tests read (q_c(x_c), accept uniforms), the
-        // final-sample uniform. (Pulling the children's drafter rows into L2 here
-        // measured slower: merge workload 62.9 vs 59.6 us per call.)
-        for (int i = u + 1 + tid; !NAIVE && i < se_u; i += kWalkThreads)
-            if (sm.depth[i] == du + 1) {
-                sm.cq[i] = __ldg(ssm + ((size_t)b * NQ + sm.qrow[i]) * V + sm.tok[i]);
-                sm.cu[i] = __ldg(u_acc + sm.perm[i]);
-            }
-        if (tid == kWalkThreads - 1) sm.us = __ldg(u_smp + sm.perm[u]);
-        const bool landed = mbar_wait_bounded(bar, visit & 1u);
+        // meanwhile: the values the tests read (q_c(x_c), accept uniforms; at
+        // most one node per thread: n <= kMaxNodes <= threads) and the
+        // final-sample uniform, into registers now and into shared memory after
+        // the passes, so that their latency hides under the passes. (Pulling the
+        // first child's drafter and target rows into L2 here measured slower:
+        // each warp's range then lands 1 us later, merge workload 54.2 vs 48.0
+        // us per call.)
+        const int ti = u + 1 + tid;
+        const bool tchild = !NAIVE && ti < se_u && sm.depth[ti] == du + 1;
+        float t_q = 0.f, t_u = 0.f;
+        if (tchild) {
+            t_q = __ldg(ssm + ((size_t)b * NQ + sm.qrow[ti]) * V + sm.tok[ti]);
+            t_u = __ldg(u_acc + sm.perm[ti]);
+        }
+        const float t_us = tid == kWalkThreads - 1 ? __ldg(u_smp + sm.perm[u]) : 0.f;
+        const bool landed = mbar_wait_warp(wbar, visit & 1u);
         ++visit;
-        // pass 1: maximum of the row (of the tempered logits: invT > 0), finiteness
-        float mx = -FLT_MAX;
-        int nf = 0;
+        // the warp's maximum (invT > 0) and finiteness: x * 0 + z stays 0 unless
+        // x is NaN or infinite
+        float mx = -FLT_MAX, z = 0.f;
         if (landed)
             for (int g = g0 + lane; g < g1; g += 32) {
                 const float4 a = R4[g];
-                nf |= !isfinite(a.x) | !isfinite(a.y) | !isfinite(a.z) | !isfinite(a.w);
                 mx = fmaxf(mx, fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)));
+                z = __fmaf_rn(a.x, 0.f, z); z = __fmaf_rn(a.y, 0.f, z);
+                z = __fmaf_rn(a.z, 0.f, z); z = __fmaf_rn(a.w, 0.f, z);
             }
-        int tmo = 0;
-        const float mxb = walk_max(sm, k++, nf ? INFINITY : mx, !landed, tmo);
-        if (tmo) { timeout = 1; break; }
-        if (mxb == INFINITY) { nonfinite = 1; break; }
-        const float m = mxb * invT;
-        // pass 2: e = 2^((l/T - m) log2 e), R = e, S = sum e; R at the first child's token
-        const int c_first = u + 1 < se_u ? u + 1 : -1;
+        mx = warp_max(mx);
+        const int nf = __any_sync(0xffffffffu, z != 0.f);
+        // e = 2^(l a2 - Mw), a2 = log2(e) / T, Mw = max(l) a2, into R (one FMA and
+        // the hardware exp2 an entry), their sum; R at the first child's token
+        const float Mw = mx * a2;
         const int x_first = (!NAIVE && c_first >= 0) ? sm.tok[c_first] : -1;
         float s = 0.f, cc = 0.f;
-        for (int g = g0 + lane; g < g1; g += 32) {
-            float4 a = R4[g];
-            a.x = e_of(a.x, invT, m); a.y = e_of(a.y, invT, m); a.z = e_of(a.z, invT, m); a.w = e_of(a.w, invT, m);
-            kahan(s, cc, a.x); kahan(s, cc, a.y); kahan(s, cc, a.z); kahan(s, cc, a.w);
-            R4[g] = a;
-            if (g == (x_first >> 2)) sm.rx[k & 1] = pick4(a, x_first & 3);
+        if (landed && !nf)
+            for (int g = g0 + lane; g < g1; g += 32) {
+                float4 a = R4[g];
+                a.x = ex2(__fmaf_rn(a.x, a2, -Mw)); a.y = ex2(__fmaf_rn(a.y, a2, -Mw));
+                a.z = ex2(__fmaf_rn(a.z, a2, -Mw)); a.w = ex2(__fmaf_rn(a.w, a2, -Mw));
+                kahan(s, cc, (a.x + a.y) + (a.z + a.w));
+                R4[g] = a;
+            }
+        __syncwarp();
+        if (lane == 0 && x_first >= 0 && (x_first >> 2) >= g0 && (x_first >> 2) < g1) sm.rx = R[x_first];
+        if (tchild) {
+            sm.cq[ti] = t_q;
+            sm.cu[ti] = t_u;
         }
-        float Sh = s, Sl = -cc;
-        int kr = k;                          // the slot of R's warp partials and of rx
-        walk_sum(sm, k++, Sh, Sl);
-        bool sums_valid = true;
+        if (tid == kWalkThreads - 1) sm.us = t_us;
+        walk_publish(sm, s, -cc, Mw, (nf ? 1 : 0) | (landed ? 0 : 2));
+        __syncthreads();
+        if (warp == 0) walk_decide_stats(sm, c_first, se_u, C4, NAIVE);
+        __syncthreads();
+        int v = sm.verdict;
+        if (v == kVTimeout) { timeout = 1; break; }
+        // R relative to each warp's maximum (factor fw) until a rejection pass
+        // rescales it to the row maximum
+        bool local = true;
+        float fw = sm.f[warp];
         // children in input order: u+1, sub_end[u+1], ... below sub_end[u]
-        int nrej = 0;
-        int accepted = -1;
-        for (int c = c_first; !NAIVE && c >= 0 && c < se_u; c = sm.sub_end[c]) {
-            const float qx = sm.cq[c];
-            if (!isfinite(qx)) { nonfinite = 1; break; }
-            const float Sf = Sh + Sl;
-            float a = 1.f;
-            if (qx > 0.f) a = fminf(1.f, sm.rx[kr & 1] / (Sf * qx));
-            const float uc = sm.cu[c];
-            if (tid == 0 && fabsf(uc - a) < (float)kLowMargin) ++sm.lowm;
-            if (uc <= a) { accepted = c; break; }
-            // rejection: R' = max(0, R - S q_c), S' = sum R'; R' at the next child's token
-            const float4 *q4 = reinterpret_cast<const float4 *>(ssm + ((size_t)b * NQ + sm.qrow[c]) * V);
+        int c = c_first;
+        while (v == kVReject) {
+            // child c rejected: R' = max(0, R - S q_c), S' = sum R'; R' at the next child's token
+            const float Sf = sm.Sh + sm.Sl;
+            const float *qc = ssm + ((size_t)b * NQ + sm.qrow[c]) * V;
+            const float4 *q4 = reinterpret_cast<const float4 *>(qc);
             const int c_next = sm.sub_end[c] < se_u ? sm.sub_end[c] : -1;
             const int x_next = c_next >= 0 ? sm.tok[c_next] : -1;
-            float s2 = 0.f, c2 = 0.f;
-            int bad = 0;
+            float s2 = 0.f, c2 = 0.f, zq = 0.f;   // zq: NaN once a drafter value is not finite
             for (int g00 = g0 + lane; g00 < g1; g00 += 4 * 32) {
                 float4 qv[4];
 #pragma unroll
@@ -947,98 +1079,76 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
                 for (int j = 0; j < 4; ++j) {
                     const int g = g00 + 32 * j;
                     if (g < g1) {
-                        bad |= !isfinite(qv[j].x) | !isfinite(qv[j].y) | !isfinite(qv[j].z) | !isfinite(qv[j].w);
+                        zq = __fmaf_rn(qv[j].x, 0.f, zq); zq = __fmaf_rn(qv[j].y, 0.f, zq);
+                        zq = __fmaf_rn(qv[j].z, 0.f, zq); zq = __fmaf_rn(qv[j].w, 0.f, zq);
                         float4 r = R4[g];
-                        r.x = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].x, r.x));
-                        r.y = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].y, r.y));
-                        r.z = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].z, r.z));
-                        r.w = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].w, r.w));
+                        r.x = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].x, r.x * fw));
+                        r.y = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].y, r.y * fw));
+                        r.z = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].z, r.z * fw));
+                        r.w = fmaxf(0.f, __fmaf_rn(-Sf, qv[j].w, r.w * fw));
                         R4[g] = r;
-                        kahan(s2, c2, r.x); kahan(s2, c2, r.y); kahan(s2, c2, r.z); kahan(s2, c2, r.w);
-                        if (g == (x_next >> 2)) sm.rx[k & 1] = pick4(r, x_next & 3);
+                        kahan(s2, c2, (r.x + r.y) + (r.z + r.w));
                     }
                 }
             }
-            // one reduction for both: a non-finite drafter value makes the sum NaN
-            float Nh = bad ? NAN : s2, Nl = bad ? 0.f : -c2;
-            const int kn = k;
-            walk_sum(sm, k++, Nh, Nl);
-            if (isnan(Nh)) { nonfinite = 1; break; }
-            if (Nh > 0.f) {
-                if (tid == 0) {
-                    sm.rej_q[nrej] = reinterpret_cast<const float *>(q4);
-                    sm.rej_S[nrej] = Sf;
-                }
-                ++nrej;
-                Sh = Nh;
-                Sl = Nl;
-                kr = kn;
-                sums_valid = true;
-            } else {
+            __syncwarp();
+            if (lane == 0 && x_next >= 0 && (x_next >> 2) >= g0 && (x_next >> 2) < g1) sm.rx = R[x_next];
+            // a non-finite drafter value makes the partial NaN
+            const bool bad = __any_sync(0xffffffffu, zq != 0.f);
+            walk_publish(sm, bad ? NAN : s2, bad ? 0.f : -c2, 0.f, 0);
+            __syncthreads();
+            if (warp == 0) walk_decide_resid(sm, qc, c_next, se_u, C4, status);
+            __syncthreads();
+            local = false;   // R is now relative to the row maximum
+            fw = 1.f;
+            v = sm.verdict;
+            if (v == kVZero) {
                 // zero normaliser: keep the residual unchanged (rebuilt from the
                 // rejections applied so far: the in-place pass overwrote it)
-                if (tid == 0) flag(status, TS_STATUS_ZERO_RESID);
-                const Resid keep{row, invT, m, sm.rej_q, sm.rej_S, nrej, nullptr};
-                for (int g = g0 + lane; g < g1; g += 32)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float v = resid_recompute(keep, 4 * g + e);
-                        R[4 * g + e] = v;
-                        if (4 * g + e == x_next) sm.rx[kn & 1] = v;
-                    }
+                const Resid keep{row, invT, sm.m, sm.rej_q, sm.rej_S, sm.nrej, nullptr};
+                float s3 = 0.f, c3 = 0.f;
+                for (int g = g0 + lane; g < g1; g += 32) {
+                    float4 r;
+                    r.x = resid_recompute(keep, 4 * g);
+                    r.y = resid_recompute(keep, 4 * g + 1);
+                    r.z = resid_recompute(keep, 4 * g + 2);
+                    r.w = resid_recompute(keep, 4 * g + 3);
+                    R4[g] = r;
+                    kahan(s3, c3, (r.x + r.y) + (r.z + r.w));
+                }
+                __syncwarp();
+                if (lane == 0 && x_next >= 0 && (x_next >> 2) >= g0 && (x_next >> 2) < g1) sm.rx = R[x_next];
+                walk_publish(sm, s3, -c3, 0.f, 0);
                 __syncthreads();
-                kr = kn;
-                sums_valid = false;
+                if (warp == 0) walk_decide_rebuilt(sm, c_next, se_u, C4);
+                __syncthreads();
+                v = sm.verdict;
             }
+            c = c_next;
         }
-        if (nonfinite) break;
-        if (accepted >= 0) {
+        if (v == kVNonfinite) { nonfinite = 1; break; }
+        if (v >= 0) {   // child v accepted
             if (tid == 0) {
-                ot[cnt] = sm.tok[accepted];
-                op[cnt + 1] = sm.perm[accepted];
+                ot[cnt] = sm.tok[v];
+                op[cnt + 1] = sm.perm[v];
             }
             ++cnt;
-            u = accepted;
+            u = v;
             continue;
         }
-        // ---- inverse CDF of the residual: the first y with C(y) > u * S
-        if (!sums_valid) {   // partials of the rebuilt residual
-            float s3 = 0.f, c3 = 0.f;
-            for (int g = g0 + lane; g < g1; g += 32) {
-                const float4 r = R4[g];
-                kahan(s3, c3, r.x); kahan(s3, c3, r.y); kahan(s3, c3, r.z); kahan(s3, c3, r.w);
-            }
-            float h3 = s3, l3 = -c3;
-            kr = k;
-            walk_sum(sm, k++, h3, l3);
-        }
-        // the warps' partial sums (lane l holds warp l's): inclusive scan, total,
-        // target = u * total, and the warp whose chunk holds it
-        const float oh = sm.red_hi[kr & 1][lane], ol = sm.red_lo[kr & 1][lane];
-        float ih = oh, il = ol;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float bh = __shfl_up_sync(0xffffffffu, ih, o), bl = __shfl_up_sync(0xffffffffu, il, o);
-            if (lane >= o) ff_add(ih, il, bh, bl);
-        }
-        const float toth = __shfl_sync(0xffffffffu, ih, 31), totl = __shfl_sync(0xffffffffu, il, 31);
-        float tgh, tgl;
-        ff_mul_f(toth, totl, sm.us, tgh, tgl);
-        const unsigned hitw = __ballot_sync(0xffffffffu, oh > 0.f && ff_gt(ih, il, tgh, tgl));
-        const unsigned posw = __ballot_sync(0xffffffffu, oh > 0.f);
-        int ws = hitw ? __ffs(hitw) - 1 : (posw ? 31 - __clz(posw) : 0);
-        const bool fallback = hitw == 0;
-        if (warp == ws) {
-            // this warp's exclusive prefix
-            float bh = __shfl_sync(0xffffffffu, ih, ws), bl = __shfl_sync(0xffffffffu, il, ws);
-            ff_add(bh, bl, -__shfl_sync(0xffffffffu, oh, ws), -__shfl_sync(0xffffffffu, ol, ws));
+        // ---- the final sample: the first y with C(y) > u * S, inside the range
+        // of warp sm.ws (the coarse level is the deciding warp's)
+        if (warp == sm.ws) {
+            const bool fallback = sm.fb;
+            const float bh = sm.bh, bl = sm.bl, tgh = sm.tgh, tgl = sm.tgl, toth = sm.toth;
             // lane j sums the float4s [g0 + j K, g0 + (j + 1) K) of the chunk
             const int K = (g1 - g0 + 31) / 32;
             const int a0 = min(g1, g0 + lane * K), a1 = min(g1, a0 + K);
             float lh = 0.f, ll = 0.f;
             for (int g = a0; g < a1; ++g) {
                 const float4 r = R4[g];
-                ff_add(lh, ll, r.x, 0.f); ff_add(lh, ll, r.y, 0.f); ff_add(lh, ll, r.z, 0.f); ff_add(lh, ll, r.w, 0.f);
+                ff_add(lh, ll, r.x * fw, 0.f); ff_add(lh, ll, r.y * fw, 0.f);
+                ff_add(lh, ll, r.z * fw, 0.f); ff_add(lh, ll, r.w * fw, 0.f);
             }
             float jh = lh, jl = ll;   // inclusive scan over the lanes
 #pragma unroll
@@ -1058,7 +1168,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
                 int chosen = -1, last_pos = -1;
                 float margin = 0.f;
                 for (int y = 4 * a0; y < 4 * a1 && chosen < 0; ++y) {
-                    const float r = R[y];
+                    const float r = R[y] * fw;
                     if (r > 0.f) {
                         float nh = ch, nl = cl;
                         ff_add(nh, nl, r, 0.f);
@@ -1089,18 +1199,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk(int32_t *out_tokens, i
         if (!NAIVE) break;
         // naive sampling: continue at the first child holding the drawn token
         int next = -1;
-        for (int c = u + 1; c < se_u; c = sm.sub_end[c])
-            if (sm.tok[c] == chosen) { next = c; break; }
+        for (int c2 = u + 1; c2 < se_u; c2 = sm.sub_end[c2])
+            if (sm.tok[c2] == chosen) { next = c2; break; }
         if (next < 0) break;
         if (tid == 0) op[cnt] = sm.perm[next];
         u = next;
         __syncthreads();   // sm.chosen is rewritten at the next node
     }
+    // a row copy may still be in flight after a timeout: each warp waits for its
+    // own (bounded) before the block exits
+    if (timeout && lane == 0) mbar_wait_bounded(wbar, (visit - 1) & 1u);
     __syncthreads();
     if (tid == 0) {
         if (timeout) {
-            // the row copy may still be in flight: wait for it (bounded) before exiting
-            mbar_wait_bounded(bar, (visit - 1) & 1u);
             out_count[b] = 0;
             flag(status, TS_STATUS_TIMEOUT);
         } else if (nonfinite) {
