@@ -23,10 +23,8 @@ namespace ts {
 namespace {
 
 // ---------------------------------------------------------------- greedy ----
-constexpr int kGreedyThreads = 256;   // >= kMaxNodes: one tree node per thread in the merge
 constexpr int kMaxSeg = 8;
 constexpr int kGreedyBulkMin = 16384;   // segments from this size on arrive by bulk copy
-static_assert(kGreedyThreads >= kMaxNodes, "the merge gives every thread at most one node");
 
 struct ArgPart {
     float val;
@@ -45,6 +43,7 @@ __device__ __forceinline__ void consider(float x, int i, float &bv, int &bi, boo
 // mode 0: scalar loads; 1: float4 loads, eight in flight per thread; 2: the
 // segment by one bulk copy into shared memory (dynamic shared memory of the
 // segment's size)
+template <int kGreedyThreads>
 __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, int32_t *out_path,
                                                            int32_t *out_count, int32_t *argmax_out,
                                                            const float *logits, ts_tree t, int V, int seg,
@@ -63,9 +62,6 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
         return;
     }
     if (v >= n) return;
-    // the merge's tree entries, fetched now so that their latency hides under
-    // the segment's (used only if this CTA merges)
-    const int w = threadIdx.x;
     const float *row = logits + ((size_t)b * n_max + v) * V;
     float bv = -FLT_MAX;
     int bi = INT_MAX;
@@ -165,7 +161,7 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
     __shared__ int s_bad;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
-    if (w < n) {
+    for (int w = threadIdx.x; w < n; w += kGreedyThreads) {
         const size_t o = (size_t)b * n_max + w;
         s_perm[w] = t.perm[o];
         s_tok[w] = t.token[o];
@@ -1272,37 +1268,36 @@ cudaError_t launch_verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t
                                  cudaStream_t s) {
     const int rows = t.B * t.n_max;
     const bool vec4 = (V % 4 == 0) && ((uintptr_t)logits % 16 == 0);
-    // bulk copies: segments for two resident CTAs per SM over all rows (at
-    // most 96 KB a segment), when a segment is large enough for one copy to
-    // beat eight 16-byte loads per thread (llama7b-shaped rows: 8.1 -> 6.8 us)
+    unsigned *counters = (unsigned *)ws;
+    ArgPart *parts = (ArgPart *)((char *)ws + ((size_t)t.B * sizeof(unsigned) + 255) / 256 * 256);
+    // bulk copies: 256-thread CTAs, segments for two resident CTAs per SM over
+    // all rows (at most 96 KB a segment), when a segment is 16 KB or more and the
+    // grid is about one wave (LLaMA-7B-shaped rows: 8.0 -> 6.8 us a call). Larger
+    // grids keep small 128-thread CTAs without shared memory: beside the
+    // attention of a long-context step they give back SMs sooner (step 369 us
+    // against 378 us with 64 KB segments, though the call alone is 15.0 against
+    // 12.1 us)
     int seg = (2 * num_sms() + rows - 1) / rows;
     seg = max(1, min(kMaxSeg, max(seg, (int)(((size_t)V * 4 + 98303) / 98304))));
     const size_t seg_bytes = (size_t)(((V >> 2) + seg - 1) / seg) * 16;
-    int mode = vec4 ? 1 : 0;
-    size_t smem = 0;
-    if (vec4 && seg_bytes >= (size_t)kGreedyBulkMin && seg_bytes <= 98304) {
-        mode = 2;
-        smem = seg_bytes;
-        cudaError_t e = cudaFuncSetAttribute(k_greedy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (vec4 && seg_bytes >= (size_t)kGreedyBulkMin && seg_bytes <= 98304 && (long long)rows * seg <= 3LL * num_sms()) {
+        cudaError_t e = cudaFuncSetAttribute(k_greedy<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)seg_bytes);
         if (e != cudaSuccess) return e;
-    } else {
-        // vocab segments per node row: as many as fit one wave of resident CTAs
-        // (a second, partial wave doubles the time of this latency-bound pass),
-        // and no segment shorter than 2048 entries
-        static int occ = 0;
-        if (occ == 0 &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_greedy, kGreedyThreads, 0) != cudaSuccess) {
-            cudaGetLastError();
-            occ = 4;
-        }
-        const int slots = num_sms() * (occ > 0 ? occ : 1);
-        seg = max(1, min(kMaxSeg, min(slots / rows, max(1, V / 2048))));
+        return launch(k_greedy<256>, dim3(t.n_max * seg, t.B), dim3(256), seg_bytes, s, out_tokens, out_path, out_count,
+                      argmax_out, logits, t, V, seg, 2, counters, parts, status);
     }
-    unsigned *counters = (unsigned *)ws;
-    ArgPart *parts = (ArgPart *)((char *)ws + ((size_t)t.B * sizeof(unsigned) + 255) / 256 * 256);
-    dim3 grid(t.n_max * seg, t.B);
-    return launch(k_greedy, grid, dim3(kGreedyThreads), smem, s, out_tokens, out_path, out_count, argmax_out, logits,
-                  t, V, seg, mode, counters, parts, status);
+    // vocab segments per node row: as many as fit one wave of resident CTAs (a
+    // second, partial wave doubles the time of this latency-bound pass), and no
+    // segment shorter than 2048 entries
+    static int occ = 0;
+    if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_greedy<128>, 128, 0) != cudaSuccess) {
+        cudaGetLastError();
+        occ = 4;
+    }
+    const int slots = num_sms() * (occ > 0 ? occ : 1);
+    seg = max(1, min(kMaxSeg, min(slots / rows, max(1, V / 2048))));
+    return launch(k_greedy<128>, dim3(t.n_max * seg, t.B), dim3(128), 0, s, out_tokens, out_path, out_count,
+                  argmax_out, logits, t, V, seg, vec4 ? 1 : 0, counters, parts, status);
 }
 
 template <bool NAIVE>
