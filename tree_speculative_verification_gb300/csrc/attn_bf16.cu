@@ -176,6 +176,8 @@ __device__ void merge_splits(const AttnArgs &a, int b, int h, int n, int S_b, co
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_constant__ CUtensorMap map_k,
                                                                    const __grid_constant__ CUtensorMap map_v,
+                                                                   const __grid_constant__ CUtensorMap map_k8,
+                                                                   const __grid_constant__ CUtensorMap map_v8,
                                                                    AttnArgs a) {
     constexpr int D = C::D, NT = C::NT, KS = C::KS, STAGES = C::STG;
     extern __shared__ unsigned char smem_raw[];
@@ -217,15 +219,29 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB) k_attn_bf16(const __grid_
     }
     __syncthreads();
     static_assert(TK == TS_PAGE_KEYS, "one key tile is one page");
+    // one tile into its stage; the chunk's last tile, when it holds fewer than
+    // TK keys, comes in 8-row pieces (one swizzle atom each), so no more than 7
+    // rows past the chunk's end are read
     auto issue = [&](int it, int row) {
         const int st = it % STAGES;
         const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
         const uint32_t bar = bar0 + 8 * st;
-        mbar_expect_tx(bar, C::STAGE_BYTES);
+        const int nv = min(TK, k_end - (k_begin + it * TK));
+        if (nv == TK) {
+            mbar_expect_tx(bar, C::STAGE_BYTES);
 #pragma unroll
-        for (int bx = 0; bx < C::BOXES; ++bx) {
-            tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, bar);
-            tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, bar);
+            for (int bx = 0; bx < C::BOXES; ++bx) {
+                tma_load_2d(kdst + bx * C::BOX_BYTES, &map_k, bx * 64, row, bar);
+                tma_load_2d(vdst + bx * C::BOX_BYTES, &map_v, bx * 64, row, bar);
+            }
+        } else {
+            mbar_expect_tx(bar, 2u * C::BOXES * (uint32_t)((nv + 7) & ~7) * 128u);
+#pragma unroll
+            for (int bx = 0; bx < C::BOXES; ++bx)
+                for (int r8 = 0; r8 < nv; r8 += 8) {
+                    tma_load_2d(kdst + bx * C::BOX_BYTES + r8 * 128, &map_k8, bx * 64, row + r8, bar);
+                    tma_load_2d(vdst + bx * C::BOX_BYTES + r8 * 128, &map_v8, bx * 64, row + r8, bar);
+                }
         }
     };
     if (tid == 0) {
@@ -569,12 +585,13 @@ struct Variant {
     int nodes, threads, smem;
     const char *name;
     const void *fn;
-    cudaError_t (*launch)(dim3, const CUtensorMap &, const CUtensorMap &, const AttnArgs &, cudaStream_t);
+    cudaError_t (*launch)(dim3, const CUtensorMap *, const AttnArgs &, cudaStream_t);
 };
 
+// maps: K and V with 64-row boxes, then K and V with 8-row boxes
 template <class C>
-cudaError_t launch_cfg(dim3 grid, const CUtensorMap &mk, const CUtensorMap &mv, const AttnArgs &a, cudaStream_t s) {
-    return launch(k_attn_bf16<C>, grid, dim3(C::THREADS), C::SMEM, s, mk, mv, a);
+cudaError_t launch_cfg(dim3 grid, const CUtensorMap *m, const AttnArgs &a, cudaStream_t s) {
+    return launch(k_attn_bf16<C>, grid, dim3(C::THREADS), C::SMEM, s, m[0], m[1], m[2], m[3], a);
 }
 
 template <class C>
@@ -697,10 +714,12 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
         return launch_attn_tq(out, q, k_cache, v_cache, prefix_len, t, H, L_max, scale, (unsigned *)ws, status, s, why,
                               pg);
     const Variant v = pick_variant(d, t.n_max);
-    CUtensorMap mk, mv;
-    // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
+    CUtensorMap maps[4];
+    // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged;
+    // 64-row boxes, and 8-row boxes for a chunk's ragged last tile
     const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
-    if (!make_map(&mk, k_cache, d, rows, TK) || !make_map(&mv, v_cache, d, rows, TK)) {
+    if (!make_map(&maps[0], k_cache, d, rows, TK) || !make_map(&maps[1], v_cache, d, rows, TK) ||
+        !make_map(&maps[2], k_cache, d, rows, 8) || !make_map(&maps[3], v_cache, d, rows, 8)) {
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
     }
@@ -731,7 +750,7 @@ cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, cons
     a.lpt = !(lp && *lp && atoi(lp) == 0);
     // split index slowest: every first (longest) chunk is dispatched before any later one
     dim3 grid(H, t.B, plan.splits);
-    return v.launch(grid, mk, mv, a, s);
+    return v.launch(grid, maps, a, s);
 }
 
 }  // namespace ts
