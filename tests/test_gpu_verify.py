@@ -230,3 +230,44 @@ def test_mss_bad_row_index():
                    d(np.array([[0, 3]], np.int32)), d(np.zeros((B, 2, n), np.float32)), 1.0, t, status=st)
     torch.cuda.synchronize()
     assert oc.item() == 0 and st.item() & api.STATUS_INDEX
+
+
+def test_mss_fast_walk_zero_residual_rebuild_and_nonfinite():
+    """The shared-memory walk (V a multiple of 4): a rejection whose residual
+    max(0, p - q) is zero everywhere keeps the residual (status ZERO_RESID) and
+    the walk goes on with the next child, then samples; compared with the
+    oracle. Request 0 accepts the second child, request 1 rejects both and
+    samples from p, request 2 meets a NaN in the second child's drafter row."""
+    V, B, n = 8, 3, 3
+    logits = np.zeros((B, n, V), np.float32)          # p uniform: 1/8 at every node
+    logits[:, 2, 6] = 2.0
+    ssm = np.full((B, 2, V), 0.6, np.float32)           # q >= p everywhere: zero residual
+    ssm[:, 1, :] = 0.125
+    ssm[:, 1, 5] = 0.3
+    ssm[2, 1, 4] = np.nan
+    q_row = np.array([[0, 0, 1]] * B, np.int32)
+    par = np.array([[-1, 0, 0]] * B, np.int32)
+    tok = np.array([[0, 3, 5]] * B, np.int32)
+    uni = np.zeros((B, 2, n), np.float32)
+    uni[:, 0, 1] = 0.9                                   # child 1: p/q = 0.208, rejected
+    uni[0, 0, 2] = 0.1                                   # child 2: p/q = 0.417, accepted for request 0
+    uni[1, 0, 2] = 0.8                                   # rejected for request 1
+    uni[2, 0, 2] = 0.8
+    uni[:, 1, 0] = 0.55                                  # the final sample at the root
+    uni[:, 1, 2] = 0.3
+    t = api.Tree(B, n)
+    d = lambda a: to_device(a, "cuda")
+    api.tree_build(t, d(tok), d(par), d(np.full(B, n, np.int32)))
+    ot = torch.full((B, n + 1), -1, dtype=torch.int32, device="cuda")
+    op = torch.full((B, n + 1), -1, dtype=torch.int32, device="cuda")
+    oc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.verify_mss(ot, op, oc, d(logits), d(ssm), d(q_row), d(uni), 1.0, t, status=st)
+    torch.cuda.synchronize()
+    ref = oracle.verify_mss(logits, ssm, q_row, uni, par, tok, [n] * B)
+    assert oc.tolist() == ref["count"].tolist()
+    assert ref["count"].tolist()[2] == 0 and ref["count"].tolist()[0] == 2 and ref["count"].tolist()[1] == 1
+    for b in range(2):
+        c = int(ref["count"][b])
+        assert ot[b, :c].tolist() == ref["tokens"][b, :c].tolist()
+    assert st.item() & api.STATUS_ZERO_RESID and st.item() & api.STATUS_NONFINITE
