@@ -148,14 +148,14 @@ __global__ void __launch_bounds__(kGreedyThreads) k_greedy(int32_t *out_tokens, 
         p.val = bv;
         p.idx = s_nf ? -1 : bi;
         parts[((size_t)b * n_max + v) * seg + sg] = p;
-        __threadfence();
-        unsigned prev = atomicAdd(&counters[b], 1u);
+        // release of this CTA's partial, acquire of the others' for the last one
+        unsigned prev;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(&counters[b]) : "memory");
         s_last = prev == (unsigned)(n * seg - 1);
     }
     __syncthreads();
     if (!s_last) return;
     // ---- last CTA of request b: merge segments, then walk (Algorithm 2, VerifyGreedy)
-    __threadfence();
     __shared__ int am[kMaxNodes];
     __shared__ int s_perm[kMaxNodes], s_tok[kMaxNodes], s_se[kMaxNodes];
     __shared__ int s_bad;
