@@ -63,6 +63,24 @@ def attention_bytes(w) -> int:
     return kv + qo
 
 
+def append_bytes(w) -> int:
+    """Bytes a launch that also appends writes on top of attention_bytes: the
+    tree's new K and V rows into the cache (the attention already counts them
+    read once)."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return int(sum(w.n_nodes_dev)) * w.H * w.d * esz * 2
+
+
+def attention_launch(s):
+    """The kernel name ncu summaries use for the step's attention launch, and
+    whether that launch also appends the new K/V rows."""
+    from tree_speculative_verification_gb300 import api
+    w = s.w
+    kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
+    fused = bool(getattr(s, "_append_in_attention", False))
+    return (kernel + "+append" if fused else kernel), fused
+
+
 def _profile_keys(path):
     kv = {}
     with open(path) as fh:
@@ -333,7 +351,8 @@ def _timed_graphs(s, kind, K, device, stream, eager=False):
     import torch
     passes = {
         "step": lambda: [s.run(kind) for _ in range(K)],
-        "attend": lambda: [s.attend() for _ in range(K)],
+        # the step's attention launch (with the KV append when it rides there)
+        "attend": lambda: [(s.attend_append() if s._append_in_attention else s.attend()) for _ in range(K)],
         "verify": lambda: [s.verify(kind) for _ in range(K)],
     }
     evs = {k: _events(2, not eager) for k in passes}
@@ -372,13 +391,14 @@ def _timed_graphs(s, kind, K, device, stream, eager=False):
     return evs, replay, mode
 
 
-def _roofline(w, t_att_ms, kernel):
+def _roofline(w, t_att_ms, kernel, fused=False):
     peak, peak_kind = _peaks()
-    abytes = attention_bytes(w)
+    abytes = attention_bytes(w) + (append_bytes(w) if fused else 0)
     achieved = abytes / (t_att_ms * 1e-3) / 1e9
     traffic, prof = _traffic_from_profile(w, kernel)
+    call = "tree_attention_append" if fused else "tree_attention"
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": traffic, "traffic_source": prof, "kernel": f"tree_attention ({kernel})",
+            "traffic": traffic, "traffic_source": prof, "kernel": f"{call} ({kernel})",
             "algorithmic_bytes_per_launch": abytes, "peak_kind": peak_kind, "avg_launch_us": t_att_ms * 1e3}
 
 
@@ -403,8 +423,8 @@ def measure_other_config(name, args, device, stream):
         torch.cuda.synchronize()
         out[k] = evs[k][0].elapsed_time(evs[k][1]) / K
     nodes = int(w.n_nodes_dev.sum())
-    kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
-    roof = _roofline(w, out["attend"], kernel)
+    kernel, fused = attention_launch(s)
+    roof = _roofline(w, out["attend"], kernel, fused)
     line = {"value": nodes / (out["step"] * 1e-3), "unit": "nodes/s", "ms_per_step": out["step"],
             "nodes_per_step": nodes, "attention_ms": out["attend"], "verify_ms": out["verify"], "verify": kind,
             "attention_kernel": kernel, "roofline_frac": roof["frac"], "attention_gbs": roof["achieved"],
@@ -483,8 +503,8 @@ def run_ours(args):
         if dist:
             dist.destroy_process_group()
         return
-    kernel = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
-    roof = _roofline(w, t_att, kernel)
+    kernel, fused = attention_launch(s)
+    roof = _roofline(w, t_att, kernel, fused)
     launches = args.steps * s.launches_per_step(kind)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     host_w = w

@@ -221,6 +221,24 @@ ts_status tree_attention(void *out, const void *q, const void *k_cache, const vo
                          cudaStream_t stream);
 
 /*
+ * tree_attention_append -- kv_append and tree_attention in one call (SpecInfer
+ * sec. 4.2: the tree's new keys and values join the KV cache in depth-first
+ * order, and every node attends to the prefix and its root path): the rows
+ * k_new / v_new [B][n_max][H][d] go to cache rows P_b + dfs(v) exactly as
+ * kv_append writes them, and out gets exactly what tree_attention computes on
+ * the appended cache. Arguments, layouts, workspace and status as for those
+ * two calls; the caches are written. For the persistent tcgen05 kernel (bf16,
+ * head_dim 128, at most 128 nodes) one launch does both: a tenth warp of each
+ * CTA copies an item's rows into the cache an item ahead of the TMA loads
+ * that read them back, so the new rows are read from HBM once; otherwise the
+ * call makes the two launches of the separate calls.
+ */
+ts_status tree_attention_append(void *out, const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                const void *v_new, const int32_t *prefix_len, const ts_tree *t, int H, int d,
+                                int L_max, ts_dtype dtype, float scale, void *ws, size_t ws_bytes,
+                                uint32_t *status, cudaStream_t stream);
+
+/*
  * verify_greedy -- VerifyGreedy of SpecInfer Algorithm 2: O(u) = argmax of
  * the target logits at u (ties to the lowest token id); from the root follow
  * the first child whose token equals O(u); at the first node without such a

@@ -27,7 +27,8 @@ PAGE_KEYS = 64   # TS_PAGE_KEYS
 EXPORTS = ("tree_build", "tree_build_chains", "kv_append", "tree_attention", "verify_greedy", "verify_mss",
            "kv_commit", "treespec_workspace_size", "treespec_workspace_init", "treespec_last_error",
            "treespec_version", "tree_attention_noalloc", "treespec_attention_kernel", "verify_naive",
-           "tree_expand_topk", "kv_append_paged", "tree_attention_paged", "kv_commit_paged", "tree_build_append")
+           "tree_expand_topk", "kv_append_paged", "tree_attention_paged", "kv_commit_paged", "tree_build_append",
+           "tree_attention_append")
 #: bytes of the scratch array compiled into the library (TS_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -68,6 +69,7 @@ def load_library(path: str | None = None):
         "kv_append": [P, P, P, P, P, T, I, I, I, I, P, P],
         "tree_build_append": [T, P, P, I, P, P, P, P, P, I, I, I, I, P, P],
         "tree_attention": [P, P, P, P, P, T, I, I, I, I, F, P, Z, P, P],
+        "tree_attention_append": [P, P, P, P, P, P, P, T, I, I, I, I, F, P, Z, P, P],
         "verify_greedy": [P, P, P, P, P, T, I, P, Z, P, P],
         "verify_mss": [P, P, P, P, P, P, I, P, P, I, P, F, T, I, P, P],
         "verify_naive": [P, P, P, P, P, P, I, P, F, T, I, P, P],
@@ -225,6 +227,19 @@ def tree_attention(out, q, k_cache, v_cache, prefix_len, tree: Tree, scale: floa
     _check(lib.tree_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(_i32(prefix_len, "prefix_len")),
                               tree.c, H, d, L_max, _dtype(k_cache), float(scale), _ptr(ws), nbytes, _ptr(status),
                               _stream(stream)), "tree_attention")
+
+
+def tree_attention_append(out, q, k_cache, v_cache, k_new, v_new, prefix_len, tree: Tree, scale: float = 0.0,
+                          ws=None, status=None, stream=None):
+    """kv_append and tree_attention in one call (one launch with the persistent
+    tcgen05 kernel, else the two launches)."""
+    lib = load_library()
+    B, H, L_max, d = k_cache.shape
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.tree_attention_append(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                     _ptr(_i32(prefix_len, "prefix_len")), tree.c, H, d, L_max, _dtype(k_cache),
+                                     float(scale), _ptr(ws), nbytes, _ptr(status), _stream(stream)),
+           "tree_attention_append")
 
 
 def tree_attention_noalloc(out, q, k_cache, v_cache, prefix_len, tree: Tree, scale: float = 0.0, status=None,

@@ -235,6 +235,46 @@ ts_status tree_attention(void *out, const void *q, const void *k_cache, const vo
     return cuda_result(e, "tree_attention");
 }
 
+ts_status tree_attention_append(void *out, const void *q, void *k_cache, void *v_cache, const void *k_new,
+                                const void *v_new, const int32_t *prefix_len, const ts_tree *t, int H, int d,
+                                int L_max, ts_dtype dtype, float scale, void *ws, size_t ws_bytes, uint32_t *status,
+                                cudaStream_t stream) {
+    ts_status st = ts::check_attention_args(out, q, k_cache, v_cache, prefix_len, t, H, d, L_max, dtype,
+                                            "tree_attention_append");
+    if (st) return st;
+    if (!k_new || !v_new) return fail(TS_ERR_INVALID_ARG, "tree_attention_append: NULL pointer");
+    if (!aligned16(k_new) || !aligned16(v_new))
+        return fail(TS_ERR_INVALID_ARG, "tree_attention_append: new K/V must be 16-byte aligned");
+    const ts::AttnPlan plan = dtype == TS_BF16 ? ts::attn_plan(t->B, H, t->n_max, d, L_max, dtype) : ts::AttnPlan{};
+    if (dtype == TS_BF16 && (!ws || ws_bytes < plan.ws_bytes))
+        return fail(TS_ERR_INVALID_ARG, "tree_attention_append: workspace of %zu bytes needed, %zu given",
+                    plan.ws_bytes, ws ? ws_bytes : (size_t)0);
+    if (dtype == TS_BF16 && !aligned16(ws))
+        return fail(TS_ERR_INVALID_ARG, "tree_attention_append: workspace must be 16-byte aligned");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d);
+    if (dtype == TS_BF16 && plan.tq) {   // one launch: the persistent kernel appends as it goes
+        const char *why = nullptr;
+        cudaError_t e = ts::launch_attn_tq(out, q, k_cache, v_cache, prefix_len, *t, H, L_max, scale, (unsigned *)ws,
+                                           status, stream, &why, ts::PagedArgs(), k_new, v_new);
+        if (why) return fail(TS_ERR_CUDA, "tree_attention_append: %s", why);
+        return cuda_result(e, "tree_attention_append");
+    }
+    const int esize = dtype == TS_BF16 ? 2 : 4;
+    cudaError_t e = ts::launch_kv_append(k_cache, v_cache, k_new, v_new, prefix_len, *t, H, d, L_max, esize, status,
+                                         stream);
+    if (e != cudaSuccess) return cuda_result(e, "tree_attention_append");
+    if (dtype == TS_F32)
+        return cuda_result(ts::launch_attn_f32((float *)out, (const float *)q, (const float *)k_cache,
+                                               (const float *)v_cache, prefix_len, *t, H, d, L_max, scale, status,
+                                               stream),
+                           "tree_attention_append");
+    const char *why = nullptr;
+    e = ts::launch_attn_bf16(out, q, k_cache, v_cache, prefix_len, *t, H, d, L_max, scale, plan, ws, status, stream,
+                             &why);
+    if (why) return fail(TS_ERR_CUDA, "tree_attention_append: %s", why);
+    return cuda_result(e, "tree_attention_append");
+}
+
 ts_status verify_greedy(int32_t *out_tokens, int32_t *out_path, int32_t *out_count, int32_t *argmax_out,
                         const float *logits, const ts_tree *t, int V, void *ws, size_t ws_bytes, uint32_t *status,
                         cudaStream_t stream) {

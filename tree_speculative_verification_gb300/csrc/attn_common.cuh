@@ -121,6 +121,10 @@ struct AttnArgs {
     const int32_t *bt = nullptr;   // paged cache: block table [B][max_pages], else dense
     int max_pages = 0, num_pages = 0;
     int lpt = 0;                   // grid rows take requests longest first
+    // tree_attention_append (dense cache, persistent kernel): the new K/V rows
+    // [B][n_max][H][d] that the kernel also writes to the cache rows P + dfs
+    const uint4 *k_new = nullptr, *v_new = nullptr;
+    uint4 *k_cache_w = nullptr, *v_cache_w = nullptr;
 };
 
 // TMA row of the 64-key tile that starts at logical key key0 of (b, h): the

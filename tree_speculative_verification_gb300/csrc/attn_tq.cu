@@ -68,7 +68,7 @@ struct TqCfg {
     static constexpr int REQ_CACHE = 512;                 // (n, P) of the first requests, in shared memory
     static constexpr int OFF_REQ = OFF_XO + 4 * 32 * XO_STRIDE * 4;
     static constexpr int RING = 4;                        // published items (the queue's shared-memory ring)
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 2 * RING;
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 3 * RING;
     static constexpr int OFF_ORDER = OFF_REQ + REQ_CACHE * 8;   // requests longest first
     static constexpr int OFF_BAR = OFF_ORDER + REQ_CACHE * 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -181,12 +181,17 @@ __device__ __forceinline__ void tq_load_q(const uint4 *src, uint32_t tmem, int q
 }
 
 // DUP: every tree of the launch has at most 64 nodes, and TMEM lanes 64-127
-// hold a second copy of rows 0-63 (see the file comment).
-template <bool DUP>
-__global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_constant__ CUtensorMap map_k,
-                                                               const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
+// hold a second copy of rows 0-63 (see the file comment). FUSED: the call
+// also appends the tree's new K/V rows to the cache (kv_append): a tenth warp
+// copies each item's rows from the new K/V into the cache rows P + dfs (an
+// item ahead of the TMA producer, which waits for them before it loads the
+// item's tiles that hold tree keys; they are then read back from L2).
+template <bool DUP, bool FUSED>
+__global__ void __launch_bounds__(TqCfg::THREADS + (FUSED ? 32 : 0), 1)
+    k_attn_tq(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
     using C = TqCfg;
     constexpr int D = C::D;
+    constexpr int NTHR = C::THREADS + (FUSED ? 32 : 0);
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sm_base = smem_u32(sm);
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
     const uint32_t full = sm_base + C::OFF_BAR, empty = full + 8 * C::STAGES;
     const uint32_t sfull = empty + 8 * C::STAGES, pfull = sfull + 16, pvdone = pfull + 16;
     const uint32_t qready = pvdone + 16, ofree = qready + 16, fin = ofree + 8;
-    const uint32_t iready = fin + 8, ifree = iready + 8 * C::RING;
+    const uint32_t iready = fin + 8, ifree = iready + 8 * C::RING, tready = ifree + 8 * C::RING;
     volatile int *ring = misc + C::MISC_RING;
 
     if (warp == 0) {
@@ -228,19 +233,21 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
         mbar_init(fin, 1);
         for (int r = 0; r < C::RING; ++r) {
             mbar_init(iready + 8 * r, 1);
-            mbar_init(ifree + 8 * r, 1 + C::SM_WARPS);   // the MMA issuer and every softmax warp
+            // the MMA issuer, every softmax warp (and the tree-row warp)
+            mbar_init(ifree + 8 * r, 1 + C::SM_WARPS + (FUSED ? 1 : 0));
+            mbar_init(tready + 8 * r, 1);   // the item's tree rows are in the cache
         }
         misc[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // every role reads the requests' (n, P) at each item: one copy in shared memory
-    for (int b = tid; b < a.t.B && b < C::REQ_CACHE; b += C::THREADS) req_s[b] = make_int2(a.t.n_nodes[b], a.prefix_len[b]);
+    for (int b = tid; b < a.t.B && b < C::REQ_CACHE; b += NTHR) req_s[b] = make_int2(a.t.n_nodes[b], a.prefix_len[b]);
     __syncthreads();
     // the producer hands out the requests' items longest first (keys P + n,
     // ties to the lower request), so that with ragged prefixes the last items
     // of the launch are short ones; request order when B exceeds the cache
     const bool lpt = a.t.B <= C::REQ_CACHE;
-    for (int b = tid; lpt && b < a.t.B; b += C::THREADS) {
+    for (int b = tid; lpt && b < a.t.B; b += NTHR) {
         const int kb = req_s[b].x > 0 ? req_s[b].x + req_s[b].y : -1;
         int rank = 0;
         for (int o = 0; o < a.t.B; ++o) {
@@ -285,9 +292,17 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
                     break;
                 }
                 const TqItem it = tq_item(a, req_s, p);
+                bool rows_ready = !FUSED;
                 for (int j = 0; j < it.ntiles; ++j, ++g) {
                     const int st = g % C::STAGES, key0 = j * C::TKT;
                     const bool h1 = key0 + C::HALF < it.L;   // the tile's second 64 keys hold any key
+                    if (!rows_ready && key0 + C::TKT > it.P) {   // the first tile with tree keys
+                        if (!mbar_wait_bounded(tready + 8 * (k % C::RING), (uint32_t)(k / C::RING) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        rows_ready = true;
+                    }
                     // rows (page ids) fetched before the wait
                     const int row0 = tile_row(a, it.b, it.h, key0);
                     const int row1 = h1 ? tile_row(a, it.b, it.h, key0 + C::HALF) : 0;
@@ -403,6 +418,54 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
             if (!mbar_wait_bounded(fin, 0)) misc[1] = 1;
         }
         __syncwarp();
+    } else if (FUSED && warp == 2 + C::SM_WARPS) {   // -------------------- tree rows into the cache
+        // item u of this CTA: its n new K/V rows (input order, 256 bytes each)
+        // to cache rows P + dfs(v), eight rows per batch with every load of a
+        // batch in flight; then a proxy fence (the TMA reads them back) and
+        // tready of the item's ring slot
+        bool ok = true;
+        for (int u = 0; ok; ++u) {
+            const int r = u % C::RING;
+            if (!mbar_wait_warp(iready + 8 * r, (uint32_t)(u / C::RING) & 1u)) {
+                ok = false;
+                break;
+            }
+            const int p = ring[r];
+            if (p >= 0) {
+                const TqItem it = tq_item(a, req_s, p);
+                const int n_max = a.t.n_max;
+                const size_t crow = ((size_t)it.b * a.H + it.h) * a.L_max + it.P;   // the item's row P
+                const int c = lane & 15;
+                for (int r0 = 0; r0 < it.n; r0 += 8) {
+                    uint4 kv[4], vv[4];
+                    size_t dst[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int v = r0 + 2 * j + (lane >> 4);
+                        dst[j] = ~(size_t)0;
+                        if (v < it.n) {
+                            const size_t src = (((size_t)it.b * n_max + v) * a.H + it.h) * (D / 8) + c;
+                            dst[j] = (crow + __ldg(a.t.dfs_of + (size_t)it.b * n_max + v)) * (D / 8) + c;
+                            kv[j] = __ldcs(a.k_new + src);
+                            vv[j] = __ldcs(a.v_new + src);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (dst[j] != ~(size_t)0) {
+                            a.k_cache_w[dst[j]] = kv[j];
+                            a.v_cache_w[dst[j]] = vv[j];
+                        }
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tready + 8 * r);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ifree + 8 * r);
+            if (p < 0) break;
+        }
+        if (!ok && lane == 0) misc[1] = 1;
     } else {   // ------------------------------------------------------ softmax
         const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int prow = quarter * 32 + lane;                  // this lane's TMEM row
@@ -673,7 +736,8 @@ __global__ void __launch_bounds__(TqCfg::THREADS, 1) k_attn_tq(const __grid_cons
 
 cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
-                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg) {
+                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg,
+                           const void *k_new, const void *v_new) {
     CUtensorMap mk, mv;
     // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
     const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
@@ -681,9 +745,14 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
     }
-    const bool dup = t.n_max <= 64;
-    cudaError_t e = cudaFuncSetAttribute(dup ? k_attn_tq<true> : k_attn_tq<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
+    const bool dup = t.n_max <= 64, fused = k_new != nullptr;
+    if (fused && pg.bt) {
+        *why = "the fused append takes a dense cache";
+        return cudaErrorInvalidValue;
+    }
+    const void *fn = fused ? (dup ? (const void *)k_attn_tq<true, true> : (const void *)k_attn_tq<false, true>)
+                           : (dup ? (const void *)k_attn_tq<true, false> : (const void *)k_attn_tq<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
     if (e != cudaSuccess) return e;
     AttnArgs a;
     a.out = (__nv_bfloat16 *)out;
@@ -703,11 +772,20 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     a.bt = pg.bt;
     a.max_pages = pg.max_pages;
     a.num_pages = pg.num_pages;
+    a.k_new = (const uint4 *)k_new;
+    a.v_new = (const uint4 *)v_new;
+    a.k_cache_w = (uint4 *)const_cast<void *>(k_cache);
+    a.v_cache_w = (uint4 *)const_cast<void *>(v_cache);
     const int pairs = t.B * H;
     const int grid = pairs < num_sms() ? pairs : num_sms();
     if (grid < 1) return cudaSuccess;
-    if (dup) return launch(k_attn_tq<true>, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
-    return launch(k_attn_tq<false>, dim3(grid), dim3(TqCfg::THREADS), TqCfg::SMEM, s, mk, mv, a);
+    const dim3 block(TqCfg::THREADS + (fused ? 32 : 0));
+    if (fused) {
+        if (dup) return launch(k_attn_tq<true, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+        return launch(k_attn_tq<false, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+    }
+    if (dup) return launch(k_attn_tq<true, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+    return launch(k_attn_tq<false, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
 }
 
 }  // namespace ts

@@ -116,9 +116,12 @@ cudaError_t launch_attn_f32(float *out, const float *q, const float *k_cache, co
                             float scale, uint32_t *status, cudaStream_t s);
 // Persistent tcgen05 kernel with 128-key tiles (head_dim 128, at most 128
 // nodes); queue = the plan's workspace (kTqQueueBytes, zero before the launch).
+// With k_new / v_new (dense cache only) the same launch also appends the new
+// K/V rows to the cache (kv_append), in a tenth warp of each CTA.
 cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *prefix_len, const ts_tree &t, int H, int L_max, float scale,
-                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg);
+                           unsigned *queue, uint32_t *status, cudaStream_t s, const char **why, const PagedArgs &pg,
+                           const void *k_new = nullptr, const void *v_new = nullptr);
 cudaError_t launch_attn_bf16(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *prefix_len, const ts_tree &t, int H, int d, int L_max,
                              float scale, const AttnPlan &plan, void *ws, uint32_t *status, cudaStream_t s,

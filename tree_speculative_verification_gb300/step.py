@@ -66,6 +66,7 @@ class DeviceStep:
         self.ws_greedy = api.workspace(api.TS_OP_VERIFY_GREEDY, B, n_max=n_max, V=w.V, device=dev)
         self._side = None   # verification stream, created on first use
         self._fused = w.tree_mode == "widths"   # tree_build_append applies
+        self._append_in_attention = False       # tree_attention_append is one launch
         self.attention = attention and w.q is not None
         if self.attention:
             bf = w.dtype == "bf16"
@@ -81,6 +82,10 @@ class DeviceStep:
             else:
                 self.k_cache = to_device(w.k_cache, dev, bf)
                 self.v_cache = to_device(w.v_cache, dev, bf)
+                # the fused append for the tcgen05 kernel's form for trees of up to 64 nodes (with more,
+                # long-context layer: 361.7 us fused against 5.6 + 347.8 us as two launches)
+                kern = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max, api.TS_BF16 if bf else api.TS_F32)
+                self._append_in_attention = kern.startswith("k_attn_tq") and w.n_max <= 64
 
     def _pages(self, rng):
         """The prefix cache scattered into randomly placed pages of PAGE_KEYS rows."""
@@ -133,6 +138,11 @@ class DeviceStep:
         api.tree_attention(self.out, self.q, self.k_cache, self.v_cache, self.prefix_len, self.tree, 0.0,
                            self.ws_attn, self.status, stream)
 
+    def attend_append(self, stream=None):
+        """kv_append and tree_attention in one call (dense cache)."""
+        api.tree_attention_append(self.out, self.q, self.k_cache, self.v_cache, self.k_new, self.v_new,
+                                  self.prefix_len, self.tree, 0.0, self.ws_attn, self.status, stream)
+
     def verify(self, kind: str | None = None, stream=None):
         kind = kind or self.w.verify
         if kind in ("greedy", "both"):
@@ -161,7 +171,21 @@ class DeviceStep:
     def run(self, kind: str | None = None, stream=None):
         """One step. Verification reads only the tree and the logits, so it runs on
         a second stream beside the KV append and the attention; the commit, which
-        needs the accepted path and the appended rows, waits for both."""
+        needs the accepted path and the appended rows, waits for both.
+
+        With the persistent tcgen05 kernel for trees of up to 64 nodes the append
+        rides in the attention launch (tree_attention_append), and the tree is
+        built on the second stream, the verification following it there as a
+        programmatic dependent launch: its CTAs take their SMs while the build
+        runs, before the persistent attention (launched on the main stream once
+        the build is done) fills every SM. Launched side by side, the attention's
+        CTAs came first and the walk ran after it (OPT-30B-shaped step 384 us;
+        built on the second stream 356 us; 369 us with the append a launch of
+        its own). Otherwise the tree is built on the main stream: greedy
+        verification (many small CTAs) forks after the append, so that the
+        attention's CTAs are placed first, MSS right after the build, and with
+        the mma.sync kernel and an expansion tree the append rides in the
+        tree_build launch (tree_build_append)."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         if not self.attention:
             self.build(main)
@@ -176,10 +200,20 @@ class DeviceStep:
             return
         if self._side is None:
             self._side = torch.cuda.Stream(self.device)
-            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
-        # greedy verification (many small CTAs) forks after the append, so that the
-        # attention's CTAs are placed first; MSS (one large CTA per request) forks
-        # right after the build and keeps its few SMs while the attention fills the rest
+            self._fork, self._built, self._join = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        side = self._side
+        if self._append_in_attention:
+            self._fork.record(main)          # the previous step's commit
+            side.wait_event(self._fork)
+            self.build(side)
+            self._built.record(side)
+            self.verify(kind, side)
+            self._join.record(side)
+            main.wait_event(self._built)
+            self.attend_append(main)
+            main.wait_event(self._join)
+            self.commit(kind, main)
+            return
         late = (kind or self.w.verify) == "greedy"
         if late and self._fused:   # expansion tree: tree_build and kv_append in one launch
             api.tree_build_append(self.tree, self.tokens, self.w.widths, self.prefix_len, self.k_cache, self.v_cache,
@@ -189,9 +223,9 @@ class DeviceStep:
             if late:
                 self.append(main)
         self._fork.record(main)
-        self._side.wait_event(self._fork)
-        self.verify(kind, self._side)
-        self._join.record(self._side)
+        side.wait_event(self._fork)
+        self.verify(kind, side)
+        self._join.record(side)
         if not late:
             self.append(main)
         self.attend(main)
@@ -205,13 +239,16 @@ class DeviceStep:
         return int(count.sum().item())
 
     def launches_per_step(self, kind: str | None = None) -> int:
+        """Kernel launches of one step: tree_build (with the append when it rides
+        there), the append when it is a launch of its own, the attention (with
+        the append when it rides there; "a+b" names a call of two launches), the
+        commit, and one launch per verification."""
         kind = kind or self.w.verify
-        attn = 0
-        if self.attention:   # "a+b" names an attention call of two launches
+        n = 1 + (2 if kind == "both" else 1)
+        if self.attention:
             w = self.w
             name = api.attention_kernel(w.B, w.H, w.n_max, w.d, w.L_max,
                                         api.TS_BF16 if w.dtype == "bf16" else api.TS_F32)
-            attn = 2 + len(name.split("+"))
-            if kind == "greedy" and self._fused:
-                attn -= 1        # kv_append rides in the tree_build launch
-        return 1 + attn + (2 if kind == "both" else 1)
+            append_rides = self._append_in_attention or (self._fused and kind == "greedy" and not self.serial_verify)
+            n += len(name.split("+")) + 1 + (0 if append_rides else 1)
+        return n
