@@ -190,6 +190,28 @@ def test_noalloc_rejects_before_touching_the_device(lib):
     assert rc == api.TS_ERR_INVALID_ARG and b"tree" in lib.treespec_last_error()
 
 
+def test_attention_append_rejects_before_touching_the_device(lib):
+    """tree_attention_append runs the checks of tree_attention and of kv_append
+    (new K/V present and 16-byte aligned, the workspace) before anything is
+    enqueued: with no GPU here a device call would come back as TS_ERR_CUDA."""
+    t = _tree()
+    p, bad = C.c_void_p(0x10000), C.c_void_p(0x10008)
+    ws = C.c_void_p(0x20000)
+    args = lambda **kw: [kw.get(k, p) for k in ("out", "q", "kc", "vc", "kn", "vn", "pl")]
+    rc = lib.tree_attention_append(*args(kn=None), C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, ws, 1 << 20, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"NULL" in lib.treespec_last_error()
+    rc = lib.tree_attention_append(*args(vn=bad), C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, ws, 1 << 20, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
+    rc = lib.tree_attention_append(*args(kc=bad), C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, ws, 1 << 20, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"aligned" in lib.treespec_last_error()
+    rc = lib.tree_attention_append(*args(), C.byref(t), 4, 128, 64, api.TS_BF16, 0.0, ws, 16, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"workspace" in lib.treespec_last_error()
+    rc = lib.tree_attention_append(*args(), C.byref(t), 4, 96, 64, api.TS_BF16, 0.0, ws, 1 << 20, None, None)
+    assert rc == api.TS_ERR_UNSUPPORTED
+    rc = lib.tree_attention_append(*args(), None, 4, 128, 64, api.TS_BF16, 0.0, ws, 1 << 20, None, None)
+    assert rc == api.TS_ERR_INVALID_ARG and b"tree" in lib.treespec_last_error()
+
+
 @pytest.mark.parametrize("B,H,n_max", [(32768, 128, 33), (8, 32, 64), (64, 56, 47)])
 def test_persistent_kernel_workspace_is_its_queue(lib, B, H, n_max, monkeypatch):
     """The persistent tcgen05 plan keeps only its item queue in the workspace,
