@@ -118,3 +118,38 @@ def test_fused_full_size(name):
     assert s.status.item() == 0
     assert _same(s.k_cache, k1) and _same(s.v_cache, v1)
     assert _same(s.out, out1)
+
+
+@pytest.mark.parametrize("d,bf16", [(64, True), (64, False), (128, False)])
+def test_two_launch_forms(d, bf16):
+    """head_dim 64 (the mma.sync kernel) and fp32: the call is kv_append then the
+    attention, with the same results as the two calls."""
+    rng = np.random.default_rng(d + 7 * bf16)
+    B, H, n_max = 2, 3, 11
+    prefix, n_nodes = [70, 5], np.array([11, 6], np.int32)
+    par = np.full((B, n_max), -1, np.int32)
+    for b in range(B):
+        for v in range(1, n_nodes[b]):
+            par[b, v] = rng.integers(0, v)
+    L_max = max(prefix) + n_max + 3
+    draw = lambda *s: rng.standard_normal(s).astype(np.float32)
+    host = [draw(B, n_max, H, d), draw(B, n_max, H, d), draw(B, n_max, H, d), draw(B, H, L_max, d),
+            draw(B, H, L_max, d)]
+    if bf16:
+        host = [f32_to_bf16_bits(a) for a in host]
+    t = api.Tree(B, n_max)
+    api.tree_build(t, to_device(np.zeros((B, n_max), np.int32), "cuda"), to_device(par, "cuda"),
+                   to_device(n_nodes, "cuda"))
+    dq, dkn, dvn, kc, vc = [to_device(a, "cuda", bf16) for a in host]
+    pl = to_device(np.asarray(prefix, np.int32), "cuda")
+    ws = api.workspace(api.TS_OP_ATTENTION, B, H, n_max, d, L_max, 1) if bf16 else None
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc1, vc1, out1 = kc.clone(), vc.clone(), torch.zeros_like(dq)
+    api.kv_append(kc1, vc1, dkn, dvn, pl, t, st)
+    api.tree_attention(out1, dq, kc1, vc1, pl, t, 0.0, ws, st)
+    kc2, vc2, out2 = kc.clone(), vc.clone(), torch.zeros_like(dq)
+    api.tree_attention_append(out2, dq, kc2, vc2, dkn, dvn, pl, t, 0.0, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    eq = (lambda a, b: torch.equal(a.view(torch.int16), b.view(torch.int16))) if bf16 else torch.equal
+    assert eq(kc1, kc2) and eq(vc1, vc2) and eq(out1, out2)
