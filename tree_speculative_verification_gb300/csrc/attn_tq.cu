@@ -37,6 +37,10 @@
 //             each writes its bf16 P over the scores it came from, loads the
 //             next item's Q rows into the other Q buffer, and at the end of an
 //             item normalises and writes its part of each output row.
+//   warp 10   (FUSED, tree_attention_append) the KV append: reads each
+//             published item and copies its new K/V rows into the cache rows
+//             P + dfs, an item ahead of the producer, which waits for them
+//             (mbarrier tready) before it loads the item's tiles with tree keys.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) (fp32 scores; P in bf16 pairs:
 // keys 0-63 at [x*128, +32) and 64-127 at [x*128+64, +32), or with DUP key block
 // kb (32 keys) at [x*128 + kb*32, +16)), O [256,384), Q0 [384,448), Q1 [448,512)
