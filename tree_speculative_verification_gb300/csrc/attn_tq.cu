@@ -18,8 +18,9 @@
 //             item ahead and publishes it in a 4-slot shared-memory ring
 //             (mbarriers iready / ifree) that the other roles read; loads
 //             128-key K and V tiles into a 3-stage ring (64 KB a stage), as
-//             64-key boxes so that a paged cache (pages of 64 keys) is read
-//             the same way, and pulls the tile after each one into L2
+//             128-key boxes, or 64-key boxes (a paged cache: one page each;
+//             and with the append in the launch), and pulls the tile after
+//             each one into L2
 //   warp 1    MMA issuer (lane 0): S = Q K^T (M = 128 node rows, N = 128 keys,
 //             K = 128 dims) with Q read from TMEM; O += P V (M = 128, N = 128
 //             dims, K = 128 keys) with P read from TMEM
@@ -190,12 +191,21 @@ __device__ __forceinline__ void tq_load_q(const uint4 *src, uint32_t tmem, int q
 // copies each item's rows from the new K/V into the cache rows P + dfs (an
 // item ahead of the TMA producer, which waits for them before it loads the
 // item's tiles that hold tree keys; they are then read back from L2).
-template <bool DUP, bool FUSED>
+// PAGED: the cache is in pages of 64 keys, each tile loaded as 64-key boxes
+// through the block table. A dense cache takes 128-key boxes (an SM moves
+// more bytes a second in fewer, larger boxes: LLaMA-7B-shaped items at batch
+// 2 26.0 -> 22.3 us, the long-context layer 347.6 -> 337.1 us; an item's last
+// tile is then loaded whole, its rows past the item's keys masked as before),
+// except with the append in the launch, which keeps 64-key boxes (the
+// OPT-30B-shaped launch measured 345.1 us with them, 352.1 us with 128-key
+// boxes, under ncu).
+template <bool DUP, bool FUSED, bool PAGED>
 __global__ void __launch_bounds__(TqCfg::THREADS + (FUSED ? 32 : 0), 1)
     k_attn_tq(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v, AttnArgs a) {
     using C = TqCfg;
     constexpr int D = C::D;
     constexpr int NTHR = C::THREADS + (FUSED ? 32 : 0);
+    constexpr bool BOX64 = PAGED || FUSED;   // 64-key boxes (else 128-key)
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sm_base = smem_u32(sm);
@@ -309,19 +319,28 @@ __global__ void __launch_bounds__(TqCfg::THREADS + (FUSED ? 32 : 0), 1)
                     }
                     // rows (page ids) fetched before the wait
                     const int row0 = tile_row(a, it.b, it.h, key0);
-                    const int row1 = h1 ? tile_row(a, it.b, it.h, key0 + C::HALF) : 0;
+                    const int row1 = BOX64 && h1 ? tile_row(a, it.b, it.h, key0 + C::HALF) : 0;
                     if (g >= C::STAGES && !mbar_wait_bounded(empty + 8 * st, (uint32_t)((g / C::STAGES) - 1) & 1u)) {
                         ok = false;
                         break;
                     }
                     const uint32_t kdst = sm_base + st * C::STAGE_BYTES, vdst = kdst + C::TILE_BYTES;
-                    mbar_expect_tx(full + 8 * st, (h1 ? 2 : 1) * 4 * C::BOX_BYTES);
-                    for (int kh = 0; kh < (h1 ? 2 : 1); ++kh) {
-                        const int row = kh ? row1 : row0;
+                    if constexpr (BOX64) {
+                        mbar_expect_tx(full + 8 * st, (h1 ? 2 : 1) * 4 * C::BOX_BYTES);
+                        for (int kh = 0; kh < (h1 ? 2 : 1); ++kh) {
+                            const int row = kh ? row1 : row0;
+#pragma unroll
+                            for (int dh = 0; dh < 2; ++dh) {
+                                tma_load_2d(kdst + dh * C::OPB + kh * C::BOX_BYTES, &map_k, dh * 64, row, full + 8 * st);
+                                tma_load_2d(vdst + dh * C::OPB + kh * C::BOX_BYTES, &map_v, dh * 64, row, full + 8 * st);
+                            }
+                        }
+                    } else {   // one 128-key box per 64-dim half of K and of V
+                        mbar_expect_tx(full + 8 * st, 8 * C::BOX_BYTES);
 #pragma unroll
                         for (int dh = 0; dh < 2; ++dh) {
-                            tma_load_2d(kdst + dh * C::OPB + kh * C::BOX_BYTES, &map_k, dh * 64, row, full + 8 * st);
-                            tma_load_2d(vdst + dh * C::OPB + kh * C::BOX_BYTES, &map_v, dh * 64, row, full + 8 * st);
+                            tma_load_2d(kdst + dh * C::OPB, &map_k, dh * 64, row0, full + 8 * st);
+                            tma_load_2d(vdst + dh * C::OPB, &map_v, dh * 64, row0, full + 8 * st);
                         }
                     }
                     {   // the tile after this one (this item's, else the next item's) into L2, so that
@@ -336,7 +355,7 @@ __global__ void __launch_bounds__(TqCfg::THREADS + (FUSED ? 32 : 0), 1)
                         }
                         if (pj >= 0 && pj < pit.ntiles) {
                             const int pk0 = pj * C::TKT;
-                            for (int kh = 0; kh < (pk0 + C::HALF < pit.L ? 2 : 1); ++kh) {
+                            for (int kh = 0; kh < (BOX64 && pk0 + C::HALF < pit.L ? 2 : 1); ++kh) {
                                 const int prow = tile_row(a, pit.b, pit.h, pk0 + kh * C::HALF);
 #pragma unroll
                                 for (int dh = 0; dh < 2; ++dh) {
@@ -745,7 +764,8 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     CUtensorMap mk, mv;
     // the TMA view: every cache row, [B*H*L_max] dense or [num_pages*H*64] paged
     const long long rows = pg.bt ? (long long)pg.num_pages * H * TS_PAGE_KEYS : (long long)t.B * H * L_max;
-    if (!make_map(&mk, k_cache, TqCfg::D, rows, TqCfg::HALF) || !make_map(&mv, v_cache, TqCfg::D, rows, TqCfg::HALF)) {
+    const int box_rows = pg.bt || k_new ? TqCfg::HALF : TqCfg::TKT;   // the kernel's BOX64
+    if (!make_map(&mk, k_cache, TqCfg::D, rows, box_rows) || !make_map(&mv, v_cache, TqCfg::D, rows, box_rows)) {
         *why = "cuTensorMapEncodeTiled failed for the KV cache";
         return cudaErrorInvalidValue;
     }
@@ -754,8 +774,10 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
         *why = "the fused append takes a dense cache";
         return cudaErrorInvalidValue;
     }
-    const void *fn = fused ? (dup ? (const void *)k_attn_tq<true, true> : (const void *)k_attn_tq<false, true>)
-                           : (dup ? (const void *)k_attn_tq<true, false> : (const void *)k_attn_tq<false, false>);
+    const bool paged = pg.bt != nullptr;
+    const void *fn = fused   ? (dup ? (const void *)k_attn_tq<true, true, false> : (const void *)k_attn_tq<false, true, false>)
+                     : paged ? (dup ? (const void *)k_attn_tq<true, false, true> : (const void *)k_attn_tq<false, false, true>)
+                             : (dup ? (const void *)k_attn_tq<true, false, false> : (const void *)k_attn_tq<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, TqCfg::SMEM);
     if (e != cudaSuccess) return e;
     AttnArgs a;
@@ -785,11 +807,15 @@ cudaError_t launch_attn_tq(void *out, const void *q, const void *k_cache, const 
     if (grid < 1) return cudaSuccess;
     const dim3 block(TqCfg::THREADS + (fused ? 32 : 0));
     if (fused) {
-        if (dup) return launch(k_attn_tq<true, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
-        return launch(k_attn_tq<false, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+        if (dup) return launch(k_attn_tq<true, true, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+        return launch(k_attn_tq<false, true, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
     }
-    if (dup) return launch(k_attn_tq<true, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
-    return launch(k_attn_tq<false, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+    if (paged) {
+        if (dup) return launch(k_attn_tq<true, false, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+        return launch(k_attn_tq<false, false, true>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+    }
+    if (dup) return launch(k_attn_tq<true, false, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
+    return launch(k_attn_tq<false, false, false>, dim3(grid), block, TqCfg::SMEM, s, mk, mv, a);
 }
 
 }  // namespace ts
