@@ -35,6 +35,15 @@ def test_tq_tile_edges(prefix):
     assert err <= TOL_BF16, err
 
 
+@pytest.mark.parametrize("n_max,prefix", [(5, 3), (30, 20)])
+def test_tq_cache_shorter_than_a_tile(n_max, prefix):
+    """One request and one head whose whole cache (at most 119 rows) is shorter
+    than one 128-key tile: the tile is loaded past the end of the cache."""
+    rng = np.random.default_rng(31 + n_max)
+    err, _, _ = _run_case(rng, 1, 1, 128, n_max, prefix=[prefix])
+    assert err <= TOL_BF16, err
+
+
 def test_tq_large_scores_rescale():
     rng = np.random.default_rng(19)
     err, _, _ = _run_case(rng, 1, 2, 128, 100, prefix=[1500], value_scale=3.0)
